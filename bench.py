@@ -1,0 +1,378 @@
+"""Benchmark of one decode step (partition pass + reduce) of paged-KV GQA decode attention.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  A step is one pass of the whole hot path over one batch:
+pda_decode (the partition kernel) then pda_reduce, both through the C ABI, inputs resident in
+HBM.  L2 is flushed (a 512 MiB write) between timed steps, outside the timed events.
+  value        (sequence, KV head) units per second, all ranks
+  e2e          the same metric through the public API with host buffers: H2D of the step's
+               query, block table and context lengths from pinned memory, the two launches,
+               D2H of the bf16 output; the KV cache is device-resident state
+  roofline     the partition kernel: algorithmic bytes per launch / its CUDA-event time,
+               against the measured copy bandwidth of the GB300 (MEASURED_PEAKS.json)
+  cpu_baseline the fp64 CPU oracle on the host cores, on a bounded sample of the same step
+Multi-GPU: replicas only (each rank runs the whole workload; no collective in the step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_gqa_block_gb300 import workloads as wl   # noqa: E402
+
+DEFAULT_WORKLOAD = wl.WORKLOAD_ORDER[1]
+METRIC = "decode seq-head-steps/s and KV-read HBM GB/s (fraction of ~8 TB/s), 1 GB300"
+UNIT = "seq-head-steps/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=wl.WORKLOAD_ORDER)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def kv_bytes_per_token_head(w: wl.Workload) -> int:
+    return 2 * w.head_dim * w.elem_bytes + (8 if w.kv_dtype == wl.KV_FP8_E4M3 else 0)
+
+
+def algorithmic_bytes(w: wl.Workload, ctx: np.ndarray, W: int) -> dict:
+    """Bytes the step must move at minimum (per step)."""
+    Hk, QG, D = w.num_kv_heads, w.query_group_size, w.head_dim
+    tok = int(ctx.sum())
+    kv = tok * Hk * kv_bytes_per_token_head(w)
+    nvalid = int(np.sum(-(-ctx.astype(np.int64) // W)))
+    q = w.num_seqs * Hk * QG * D * 2
+    bt = int(np.sum(-(-ctx.astype(np.int64) // w.kv_block_size))) * 4
+    partials = nvalid * Hk * QG * (D * 4 + 8)
+    out = w.num_seqs * Hk * QG * D * 2
+    return {"kv": kv, "decode": kv + q + bt + 4 * w.num_seqs + partials, "reduce": 2 * partials + out,
+            "tokens": tok, "units": w.num_seqs * Hk}
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_gqa_block_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM traffic per launch of the partition kernel from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        d = json.load(open(path))
+    except Exception:
+        return None
+    e = d.get(workload)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.samples = []
+        if self.proc is None:
+            return
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                try:
+                    self.samples.append({"sm": float(parts[0]), "max": float(parts[1]), "power": float(parts[2]),
+                                         "hw_slowdown": parts[4], "hw_thermal": parts[5], "sw_thermal": parts[6],
+                                         "sw_power_cap": parts[7]})
+                except ValueError:
+                    pass
+
+    def summary(self):
+        s = getattr(self, "samples", [])
+        if not s:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm_max = max(x["max"] for x in s)
+        load = [x for x in s if x["power"] > 0.25 * max(y["power"] for y in s)] or s
+        reasons = set()
+        for x in s:
+            for k in ("hw_slowdown", "hw_thermal", "sw_thermal", "sw_power_cap"):
+                if x[k].lower() == "active":
+                    reasons.add(k)
+        return {"sm_mhz": statistics.median(x["sm"] for x in load), "sm_max_mhz": sm_max,
+                "reasons": sorted(reasons), "samples": len(s)}
+
+
+# ------------------------------------------------------------------------------------ oracle leg
+def oracle_units_per_s(inp: wl.Inputs, budget_s: float, rng_seed: int = 0):
+    """The fp64 oracle as it stands, on the host cores, on a random sample of (sequence, KV head)
+    units of the step sized to about budget_s seconds.  Returns (units/s, threads, description)."""
+    import oracle
+    from tests import oracle_helpers as oh
+    oracle.build()
+    w = inp.workload
+    rng = np.random.default_rng(rng_seed)
+    order = rng.permutation(w.num_seqs * w.num_kv_heads)
+    cores = os.cpu_count() or 1
+    n = min(len(order), cores)
+    t0 = time.perf_counter()
+    r = oh.run_oracle(inp, units=order[:n], threads=cores)
+    dt = time.perf_counter() - t0
+    done, threads = n, r["threads"]
+    if dt < budget_s and n < len(order):
+        more = int(min(len(order) - n, max(1, n * (budget_s - dt) / max(dt, 1e-3))))
+        t1 = time.perf_counter()
+        r = oh.run_oracle(inp, units=order[n:n + more], threads=cores)
+        dt += time.perf_counter() - t1
+        done += more
+        threads = max(threads, r["threads"])
+    return done / dt, threads, f"{done} of {len(order)} (sequence, KV head) units drawn at random, {dt:.1f} s"
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.generate(w)
+    import oracle
+    from tests import oracle_helpers as oh
+    oracle.build()
+    cores = os.cpu_count() or 1
+    order = np.random.default_rng(0).permutation(w.num_seqs * w.num_kv_heads)
+    # size each step so that warmup + steps stay within ~2 minutes
+    t0 = time.perf_counter()
+    oh.run_oracle(inp, units=order[:cores], threads=cores)
+    per_batch = time.perf_counter() - t0
+    per_step_budget = max(0.002, 120.0 / max(1, args.steps + args.warmup))
+    n = max(1, min(len(order), int(cores * per_step_budget / max(per_batch, 1e-6))))
+    times, threads = [], 0
+    for i in range(args.warmup + args.steps):
+        units = np.roll(order, -i * n)[:n]
+        t = time.perf_counter()
+        r = oh.run_oracle(inp, units=units, threads=cores)
+        dt = time.perf_counter() - t
+        threads = max(threads, r["threads"])
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = n * len(times) / total
+    sample = f"{n} of {len(order)} (sequence, KV head) units per step, fp64, {threads} threads"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "global_batch": w.num_seqs, "num_kv_heads": w.num_kv_heads,
+                   "query_group_size": w.query_group_size, "kv_dtype": "bf16" if w.kv_dtype == 0 else "fp8_e4m3"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+# ------------------------------------------------------------------------------------ our leg
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import paged_kv_gqa_block_gb300 as pda
+    from paged_kv_gqa_block_gb300 import _build
+    _build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.generate(w)
+    p = pda.plan(w.num_seqs, w.num_kv_heads, w.query_group_size, w.kv_block_size, w.max_blocks_per_seq,
+                 w.tile_groups_per_partition, w.max_partitions, w.kv_dtype, w.softmax_scale)
+    q = torch.from_numpy(inp.query.view(np.int16)).to(dev).view(torch.bfloat16)
+    cache = torch.from_numpy(inp.cache).to(dev)
+    bt = torch.from_numpy(inp.block_table).to(dev)
+    ctx = torch.from_numpy(inp.context_lens).to(dev)
+    ws = pda.workspace(p, dev)
+    out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    B_units = w.num_seqs * w.num_kv_heads
+
+    def step():
+        pda.decode(p, q, cache, w.num_cache_blocks, bt, ctx, ws["partial_out"], ws["exp_sums"], ws["max_logits"],
+                   err_word=err, stream=stream)
+        pda.reduce(p, ctx, ws["partial_out"], ws["exp_sums"], ws["max_logits"], out, err_word=err, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())}")
+
+    # ---- device-resident timing: events around each step on the launching stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            a, m, b = ev[i]
+            a.record(stream)
+            pda.decode(p, q, cache, w.num_cache_blocks, bt, ctx, ws["partial_out"], ws["exp_sums"],
+                       ws["max_logits"], err_word=err, stream=stream)
+            m.record(stream)
+            pda.reduce(p, ctx, ws["partial_out"], ws["exp_sums"], ws["max_logits"], out, err_word=err, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if dist:
+        dist.barrier()
+    t_step = [a.elapsed_time(b) * 1e-3 for a, _, b in ev]
+    t_dec = [a.elapsed_time(m) * 1e-3 for a, m, _ in ev]
+    mean_step, mean_dec = sum(t_step) / len(t_step), sum(t_dec) / len(t_dec)
+    if dist:
+        tt = torch.tensor([mean_step, mean_dec], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        mean_step, mean_dec = float(tt[0]), float(tt[1])
+
+    # ---- end to end through the public API with host buffers
+    qh = torch.from_numpy(inp.query.view(np.int16)).view(torch.bfloat16).pin_memory()
+    bth = torch.from_numpy(inp.block_table).pin_memory()
+    ctxh = torch.from_numpy(inp.context_lens).pin_memory()
+    outh = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(10, min(args.steps, 500))
+    e2e = []
+    for i in range(e2e_steps + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        q.copy_(qh, non_blocking=True)
+        bt.copy_(bth, non_blocking=True)
+        ctx.copy_(ctxh, non_blocking=True)
+        step()
+        outh.copy_(out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            e2e.append(a.elapsed_time(b) * 1e-3)
+    mean_e2e = sum(e2e) / len(e2e)
+    if dist:
+        tt = torch.tensor([mean_e2e], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        mean_e2e = float(tt[0])
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())}")
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    ab = algorithmic_bytes(w, inp.context_lens, p.partition_tokens)
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks and peaks.get("hbm_gbs") else FALLBACK_HBM_GBS
+    achieved = ab["decode"] / mean_dec / 1e9
+    kv_gbs = ab["kv"] / mean_step / 1e9
+    res = {
+        "metric": METRIC, "value": world * B_units / mean_step, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.kv_dtype == wl.KV_BF16 else "fp8_e4m3",
+        "data": "synthetic",
+        "config": {"workload": w.name, "global_batch": world * w.num_seqs, "num_kv_heads": w.num_kv_heads,
+                   "query_group_size": w.query_group_size, "kv_block_size": w.kv_block_size,
+                   "tile_groups_per_partition": p.resolved_tile_groups, "num_partitions": p.num_partitions,
+                   "context_tokens": ab["tokens"], "seq_len_max": int(inp.context_lens.max()),
+                   "parallelism": f"replicas{world}", "l2": "flushed between timed steps (512 MiB write)"},
+        "kv_read_gbs": kv_gbs * world,
+        "kv_read_frac_of_8tbs": kv_gbs / NOMINAL_HBM_GBS,
+        "kv_read_frac_of_measured": kv_gbs / peak,
+        "decode_ms": mean_dec * 1e3,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": committed_traffic(w.name), "kernel": "pda_partition_kernel",
+                     "algorithmic_bytes_per_launch": ab["decode"],
+                     "peak_source": "measured" if peaks else "fallback"},
+        "e2e": {"value": world * B_units / mean_e2e, "unit": UNIT,
+                "h2d_bytes_per_step": int(qh.numel() * 2 + bth.numel() * 4 + ctxh.numel() * 4),
+                "d2h_bytes_per_step": int(outh.numel() * 2)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline and world >= 1:
+        v, threads, sample = oracle_units_per_s(inp, args.cpu_budget_s)
+        res["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+    print(json.dumps(res))
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,154 @@
+/*
+ * pda.h -- C ABI of libpda: single-token decode attention over a paged KV cache with GQA
+ * grouping ("paged decode attention"), for NVIDIA GB300 (sm_103a).
+ *
+ * One decode step, for every sequence b and KV head h: the query_group_size (QG) query rows
+ * of head group h (query heads h*QG .. h*QG+QG-1) attend over the sequence's context
+ * (context_lens[b] tokens), gathered through the block table in kv_block_size-token blocks.
+ * The context is split FA-2 style into partitions of G*256 tokens; pda_decode computes one
+ * partial per non-empty partition (normalised output, running max, sum of exponentials) and
+ * pda_reduce combines the partials into the softmax-weighted sum of V.
+ *
+ * Source of the method: the vLLM "tq_decode" page (build_tq_decode_module and the kernel body
+ * tq_decode_kernel): argument list, grid (sequence, KV head, partition), block-table walk,
+ * partition split with tile_groups_per_partition, mask, online softmax and partial epilogue.
+ * The KV element formats here are bf16, or fp8 e4m3 with one fp32 scale per token per KV head.
+ *
+ * Conventions for every call
+ *   - Pointers named "device" are device pointers owned by the caller; the library allocates
+ *     nothing, frees nothing and keeps no per-call state.  The only process-wide state is a
+ *     cache of the driver's tensor-map encoder and of per-device occupancy figures.
+ *   - Launches are asynchronous on the caller's stream (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream).  Calls that share output or workspace buffers race
+ *     if they overlap on the GPU.
+ *   - Every call returns a pda_status.  Argument errors are reported before anything is
+ *     launched.  Errors found in the data on the device (a context length or a block id out
+ *     of range, a pipeline wait that timed out) never fault or trap: the kernel sets a bit
+ *     in the optional device word *err_word (atomicOr) and carries on with the rule stated
+ *     at pda_decode; the caller reads the word after synchronising.
+ */
+#ifndef PDA_H
+#define PDA_H
+
+#if defined(__GNUC__)
+#define PDA_API __attribute__((visibility("default")))
+#else
+#define PDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pda_status {
+    PDA_OK = 0,
+    PDA_ERR_INVALID_ARG = -1,         /* null pointer, bad size, misaligned buffer, edited plan */
+    PDA_ERR_UNSUPPORTED = -2,         /* QG not in {6,8,16}, BS not in {16,32}, head_dim != 128 */
+    PDA_ERR_WORKSPACE_TOO_SMALL = -3, /* a size passed with a buffer is below the plan's need */
+    PDA_ERR_LAUNCH = -4,              /* the CUDA launch (or tensor-map encode) failed */
+    PDA_ERR_NOT_IMPLEMENTED = -5,
+    PDA_ERR_CUDA = -6                 /* a CUDA runtime query failed (no device, ...) */
+} pda_status;
+
+enum { PDA_KV_BF16 = 0, PDA_KV_FP8_E4M3 = 1 };
+enum { PDA_OUT_BF16 = 0, PDA_OUT_F32 = 1 };
+
+/* Bits of the device error word. */
+enum {
+    PDA_ERRW_BAD_CONTEXT_LEN = 1,   /* context_lens[b] < 0 or > max_blocks_per_seq*kv_block_size */
+    PDA_ERRW_BAD_BLOCK_ID = 2,      /* a block-table entry used by the context is outside [0, NB) */
+    PDA_ERRW_PIPELINE_TIMEOUT = 4   /* a bounded wait inside the kernel gave up */
+};
+
+/*
+ * Problem description.  The caller fills the input fields and calls pda_plan, which checks
+ * them and fills the output fields.  The launch calls recompute the outputs from the inputs
+ * and reject a plan whose outputs were edited (PDA_ERR_INVALID_ARG).
+ * Field names follow build_tq_decode_module's arguments.
+ */
+typedef struct pda_plan_t {
+    /* ---- inputs ---- */
+    int num_seqs;                  /* B >= 0 (0 = nothing to do)                                  */
+    int num_kv_heads;              /* Hk >= 1                                                      */
+    int query_group_size;          /* QG = query heads / KV heads, one of 6, 8, 16                */
+    int head_dim;                  /* D, must be 128                                              */
+    int kv_block_size;             /* BS tokens per cache block, 16 or 32                         */
+    int max_blocks_per_seq;        /* MB, row length of the block table, >= 1                     */
+    int tile_groups_per_partition; /* G >= 1, or 0 = smallest G with num_partitions <= max_partitions */
+    int max_partitions;            /* cap used when G == 0 (0 = no cap, i.e. G = 1)              */
+    int kv_dtype;                  /* PDA_KV_BF16 or PDA_KV_FP8_E4M3                              */
+    float softmax_scale;           /* <= 0 selects 1/sqrt(head_dim)                                */
+    /* ---- outputs of pda_plan ---- */
+    int num_partitions;            /* P = ceil(MB*BS / W)                                          */
+    int partition_tokens;          /* W = G * 256                                                 */
+    int resolved_tile_groups;      /* G actually used                                              */
+    float resolved_softmax_scale;
+    long long cache_block_bytes;   /* bytes per cache block (data region + metadata region)       */
+    long long meta_offset_bytes;   /* offset of the metadata region inside a block                */
+    long long workspace_bytes;     /* bytes of partial_out + exp_sums + max_logits                 */
+} pda_plan_t;
+
+/*
+ * pda_plan -- host only; launches nothing.
+ * Checks the inputs (build_tq_decode_module's asserts: QG in {6,8,16}, BS in {16,32}, G >= 1)
+ * and fills the outputs.  G == 0 follows the long-context launcher policy described with
+ * tile_groups_per_partition on the same page: the smallest G with ceil(MB*BS / (G*256)) <=
+ * max_partitions (the page's example: BS 32, cap 32 partitions -> G = 5, 32*5*256 = 40960
+ * tokens).  Also rejects sizes whose index arithmetic would not fit the kernels' int32/int64
+ * ranges (PDA_ERR_INVALID_ARG).
+ *
+ * Cache block layout (the page's stride block; formats of this library):
+ *   data region   [BS slots][Hk heads][K: D elements | V: D elements], elements bf16 or e4m3,
+ *   meta region   at meta_offset_bytes, fp8 only: fp32 [Hk][2: K scale, V scale][BS].
+ *   cache_block_bytes = BS*Hk*2*D*elem (+ Hk*2*BS*4 for fp8).
+ * Returns PDA_OK, PDA_ERR_INVALID_ARG or PDA_ERR_UNSUPPORTED.
+ */
+PDA_API int pda_plan(pda_plan_t* plan);
+
+/*
+ * pda_decode -- the partition pass (tq_decode_kernel: steps B to G).
+ *   query          device, bf16 [B][Hk*QG][D] contiguous, 16-byte aligned.
+ *   kv_cache       device, bytes [num_cache_blocks][cache_block_bytes], 16-byte aligned.
+ *   num_cache_blocks  NB >= 1, < 2^31; block ids outside [0, NB) are data errors.
+ *   block_table    device, int32 [B][max_blocks_per_seq]; only entries t/BS for t < ctx are read.
+ *   context_lens   device, int32 [B], each in [0, MB*BS].
+ *   partial_out    device, fp32 [B][Hk][P][QG][D]   (normalised partial o_p)
+ *   exp_sums       device, fp32 [B][Hk][P][QG]      (l_p = sum of exp(s - m_p) over the partition)
+ *   max_logits     device, fp32 [B][Hk][P][QG]      (m_p = max of s = softmax_scale * q.k)
+ *   err_word       device int or NULL.
+ *   stream         cudaStream_t or NULL.
+ * Only partitions p < ceil(ctx_b / W) are written; rows >= QG do not exist in the layout;
+ * other partitions' slots are left untouched.
+ * Data errors: a context length out of range is treated as 0 (nothing written for that
+ * sequence) and sets PDA_ERRW_BAD_CONTEXT_LEN; a block id out of range is read as zeros
+ * (the tensor copy's out-of-bounds fill) and sets PDA_ERRW_BAD_BLOCK_ID.
+ */
+PDA_API int pda_decode(const pda_plan_t* plan, const void* query, const void* kv_cache, long long num_cache_blocks,
+               const int* block_table, const int* context_lens, float* partial_out, float* exp_sums,
+               float* max_logits, int* err_word, void* stream);
+
+/*
+ * pda_reduce -- combines the partials of pda_decode (the reduce that follows the partition
+ * pass; the page's per-partition exp_sums / max_logits outputs exist for it):
+ *   M = max_p m_p,  w_p = l_p * exp(m_p - M),  out = sum_p (w_p / sum_q w_q) * o_p
+ * over p < ceil(ctx_b / W).  One partition is copied bit for bit; ctx 0 gives 0.
+ *   out            device, [B][Hk*QG][D], bf16 (PDA_OUT_BF16, round to nearest even) or fp32.
+ * A context length out of range gives 0 and sets PDA_ERRW_BAD_CONTEXT_LEN.
+ */
+PDA_API int pda_reduce(const pda_plan_t* plan, const int* context_lens, const float* partial_out,
+               const float* exp_sums, const float* max_logits, void* out, int out_dtype, int* err_word,
+               void* stream);
+
+/* Human-readable name of a pda_status value (static string; never NULL). */
+PDA_API const char* pda_status_string(int status);
+
+/* plan->workspace_bytes after pda_plan (-1 for a NULL or unplanned plan). */
+PDA_API long long pda_workspace_size(const pda_plan_t* plan);
+
+/* sizeof(pda_plan_t), for bindings that mirror the structure. */
+PDA_API int pda_plan_struct_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PDA_H */

@@ -1,1 +1,190 @@
-"""paged_kv_gqa_block_gb300: single-token paged-KV GQA decode attention for GB300 (sm_103a)."""
+"""paged_kv_gqa_block_gb300: single-token paged-KV GQA decode attention for GB300 (sm_103a).
+
+Thin binding over the C ABI of ``libpda.so`` (declared in ``include/pda.h``): it checks and
+marshals torch tensors into device pointers and calls the library.  Every step of the
+computation runs in the library's CUDA kernels; there is no CPU or PyTorch fallback, and a
+missing library raises.  PyTorch provides device memory and streams only.
+
+    p   = plan(num_seqs=..., num_kv_heads=..., query_group_size=8, kv_block_size=16,
+               max_blocks_per_seq=..., tile_groups_per_partition=1)
+    ws  = workspace(p, device)                    # partial_out, exp_sums, max_logits
+    decode(p, query, kv_cache, num_cache_blocks, block_table, context_lens, **ws)
+    reduce(p, context_lens, out=out, **ws)        # or decode_step(...) for both
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpda.so")
+
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+OUT_BF16 = 0
+OUT_F32 = 1
+ERRW_BAD_CONTEXT_LEN = 1
+ERRW_BAD_BLOCK_ID = 2
+ERRW_PIPELINE_TIMEOUT = 4
+HEAD_DIM = 128
+
+STATUS = {0: "PDA_OK", -1: "PDA_ERR_INVALID_ARG", -2: "PDA_ERR_UNSUPPORTED", -3: "PDA_ERR_WORKSPACE_TOO_SMALL",
+          -4: "PDA_ERR_LAUNCH", -5: "PDA_ERR_NOT_IMPLEMENTED", -6: "PDA_ERR_CUDA"}
+
+
+class PdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class Plan(ctypes.Structure):
+    """Mirror of pda_plan_t."""
+    _fields_ = [
+        ("num_seqs", ctypes.c_int), ("num_kv_heads", ctypes.c_int), ("query_group_size", ctypes.c_int),
+        ("head_dim", ctypes.c_int), ("kv_block_size", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
+        ("tile_groups_per_partition", ctypes.c_int), ("max_partitions", ctypes.c_int), ("kv_dtype", ctypes.c_int),
+        ("softmax_scale", ctypes.c_float),
+        ("num_partitions", ctypes.c_int), ("partition_tokens", ctypes.c_int), ("resolved_tile_groups", ctypes.c_int),
+        ("resolved_softmax_scale", ctypes.c_float),
+        ("cache_block_bytes", ctypes.c_longlong), ("meta_offset_bytes", ctypes.c_longlong),
+        ("workspace_bytes", ctypes.c_longlong),
+    ]
+
+    def as_dict(self) -> dict:
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_lib = None
+_lock = threading.Lock()
+_VP = ctypes.c_void_p
+
+
+def lib():
+    """The loaded libpda.so.  Raises if it has not been built (no fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(LIB_PATH)
+            P = ctypes.POINTER(Plan)
+            L.pda_plan.argtypes = [P]
+            L.pda_plan.restype = ctypes.c_int
+            L.pda_decode.argtypes = [P, _VP, _VP, ctypes.c_longlong, _VP, _VP, _VP, _VP, _VP, _VP, _VP]
+            L.pda_decode.restype = ctypes.c_int
+            L.pda_reduce.argtypes = [P, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, _VP, _VP]
+            L.pda_reduce.restype = ctypes.c_int
+            L.pda_status_string.argtypes = [ctypes.c_int]
+            L.pda_status_string.restype = ctypes.c_char_p
+            L.pda_workspace_size.argtypes = [P]
+            L.pda_workspace_size.restype = ctypes.c_longlong
+            L.pda_plan_struct_size.argtypes = []
+            L.pda_plan_struct_size.restype = ctypes.c_int
+            if L.pda_plan_struct_size() != ctypes.sizeof(Plan):
+                raise RuntimeError("pda_plan_t layout mismatch between include/pda.h and the binding")
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pda_status_string(status).decode()
+
+
+def plan(num_seqs: int, num_kv_heads: int, query_group_size: int, kv_block_size: int, max_blocks_per_seq: int,
+         tile_groups_per_partition: int = 1, max_partitions: int = 0, kv_dtype: int = KV_BF16,
+         softmax_scale: float = 0.0, head_dim: int = HEAD_DIM) -> Plan:
+    p = Plan(num_seqs, num_kv_heads, query_group_size, head_dim, kv_block_size, max_blocks_per_seq,
+             tile_groups_per_partition, max_partitions, kv_dtype, softmax_scale)
+    rc = lib().pda_plan(ctypes.byref(p))
+    if rc != 0:
+        raise PdaError(rc, "pda_plan")
+    return p
+
+
+def partial_shapes(p: Plan):
+    B, Hk, P, QG = p.num_seqs, p.num_kv_heads, p.num_partitions, p.query_group_size
+    return (B, Hk, P, QG, p.head_dim), (B, Hk, P, QG)
+
+
+def workspace(p: Plan, device, fill: float | None = None) -> dict:
+    """partial_out / exp_sums / max_logits for one step (allocated by torch)."""
+    so, ss = partial_shapes(p)
+    mk = (lambda s: torch.empty(s, dtype=torch.float32, device=device)) if fill is None else \
+        (lambda s: torch.full(s, fill, dtype=torch.float32, device=device))
+    return {"partial_out": mk(so), "exp_sums": mk(ss), "max_logits": mk(ss)}
+
+
+def _need(t: torch.Tensor, name: str, dtype, numel: int):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() * t.element_size() < numel:
+        raise ValueError(f"{name} is too small ({t.numel() * t.element_size()} < {numel} bytes)")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream if isinstance(s, torch.cuda.Stream) else int(s))
+
+
+def decode(p: Plan, query, kv_cache, num_cache_blocks: int, block_table, context_lens, partial_out, exp_sums,
+           max_logits, err_word=None, stream=None) -> None:
+    """pda_decode: the partition pass (see include/pda.h)."""
+    B, Hk, QG, D, P = p.num_seqs, p.num_kv_heads, p.query_group_size, p.head_dim, p.num_partitions
+    args = (
+        _need(query, "query", (torch.bfloat16, torch.int16, torch.uint16), B * Hk * QG * D * 2),
+        _need(kv_cache, "kv_cache", None, num_cache_blocks * p.cache_block_bytes),
+        ctypes.c_longlong(num_cache_blocks),
+        _need(block_table, "block_table", torch.int32, B * p.max_blocks_per_seq * 4),
+        _need(context_lens, "context_lens", torch.int32, B * 4),
+        _need(partial_out, "partial_out", torch.float32, B * Hk * P * QG * D * 4),
+        _need(exp_sums, "exp_sums", torch.float32, B * Hk * P * QG * 4),
+        _need(max_logits, "max_logits", torch.float32, B * Hk * P * QG * 4),
+        None if err_word is None else _need(err_word, "err_word", torch.int32, 4),
+        _stream(stream),
+    )
+    rc = lib().pda_decode(ctypes.byref(p), *args)
+    if rc != 0:
+        raise PdaError(rc, "pda_decode")
+
+
+def reduce(p: Plan, context_lens, partial_out, exp_sums, max_logits, out, err_word=None, stream=None) -> None:
+    """pda_reduce: combines the partials into out [B][Hk*QG][D] (bf16 or fp32 by out's dtype)."""
+    B, Hk, QG, D, P = p.num_seqs, p.num_kv_heads, p.query_group_size, p.head_dim, p.num_partitions
+    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    args = (
+        _need(context_lens, "context_lens", torch.int32, B * 4),
+        _need(partial_out, "partial_out", torch.float32, B * Hk * P * QG * D * 4),
+        _need(exp_sums, "exp_sums", torch.float32, B * Hk * P * QG * 4),
+        _need(max_logits, "max_logits", torch.float32, B * Hk * P * QG * 4),
+        _need(out, "out", (torch.float32, torch.bfloat16), B * Hk * QG * D * out.element_size()),
+        ctypes.c_int(out_dtype),
+        None if err_word is None else _need(err_word, "err_word", torch.int32, 4),
+        _stream(stream),
+    )
+    rc = lib().pda_reduce(ctypes.byref(p), *args)
+    if rc != 0:
+        raise PdaError(rc, "pda_reduce")
+
+
+def decode_step(p: Plan, query, kv_cache, num_cache_blocks: int, block_table, context_lens, ws: dict | None = None,
+                out=None, out_dtype=torch.bfloat16, err_word=None, stream=None):
+    """pda_decode then pda_reduce on one stream; returns out [B][Hk*QG][D]."""
+    if ws is None:
+        ws = workspace(p, query.device)
+    if out is None:
+        out = torch.empty((p.num_seqs, p.num_kv_heads * p.query_group_size, p.head_dim), dtype=out_dtype,
+                          device=query.device)
+    decode(p, query, kv_cache, num_cache_blocks, block_table, context_lens, ws["partial_out"], ws["exp_sums"],
+           ws["max_logits"], err_word=err_word, stream=stream)
+    reduce(p, context_lens, ws["partial_out"], ws["exp_sums"], ws["max_logits"], out, err_word=err_word,
+           stream=stream)
+    return out

@@ -1,0 +1,287 @@
+// pda_api.cu -- host side of libpda: pda_plan, argument checks, tensor-map encoding, launches,
+// and the reduce kernel that combines the partition partials.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "pda.h"
+#include "pda_internal.h"
+#include "pda_ptx.cuh"
+
+namespace pda {
+
+// ------------------------------------------------------------------------- reduce kernel
+// One CTA per (sequence, KV head); thread (q, d4) combines four output elements of query row q.
+//   M = max_p m_p,  w_p = l_p * e^(m_p - M),  out = sum_p (w_p / sum w) * o_p,  p < ceil(ctx / W).
+// With one partition w_0 / w_0 == 1 exactly, so the partial is copied bit for bit.
+__global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
+    const int unit = blockIdx.x;
+    const int b = unit / r.Hk, h = unit - b * r.Hk;
+    const int q = threadIdx.x >> 5, d4 = (threadIdx.x & 31) << 2;
+    if (q >= r.QG) return;
+    int ctx = __ldg(r.context_lens + b);
+    if (ctx < 0 || ctx > r.MB * r.BS) {
+        if (h == 0 && threadIdx.x == 0 && r.err_word) atomicOr(r.err_word, PDA_ERRW_BAD_CONTEXT_LEN);
+        ctx = 0;
+    }
+    const int nv = (ctx + r.W - 1) / r.W;
+    const long long base = (long long)unit * r.P * r.QG + q;   // index of (unit, p = 0, q)
+    constexpr float kLog2e = 1.4426950408889634f;
+    float M = -INFINITY;
+    for (int p = 0; p < nv; ++p) M = fmaxf(M, __ldg(r.max_logits + base + (long long)p * r.QG));
+    float wsum = 0.f;
+    for (int p = 0; p < nv; ++p) {
+        const long long i = base + (long long)p * r.QG;
+        wsum += __ldg(r.exp_sums + i) * ex2((__ldg(r.max_logits + i) - M) * kLog2e);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < nv; ++p) {
+        const long long i = base + (long long)p * r.QG;
+        const float coef = __ldg(r.exp_sums + i) * ex2((__ldg(r.max_logits + i) - M) * kLog2e) / wsum;
+        const float4 o = __ldg(reinterpret_cast<const float4*>(r.partial_out + i * kHeadDim + d4));
+        acc.x += coef * o.x;
+        acc.y += coef * o.y;
+        acc.z += coef * o.z;
+        acc.w += coef * o.w;
+    }
+    const long long orow = (long long)b * r.Hk * r.QG + (long long)h * r.QG + q;
+    if (r.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(r.out) + orow * kHeadDim + d4) = acc;
+    } else {
+        uint2 v;
+        v.x = pack_bf16(acc.x, acc.y);
+        v.y = pack_bf16(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(r.out) + orow * kHeadDim + d4) = v;
+    }
+}
+
+int launch_reduce(const ReduceArgs& r, cudaStream_t stream) {
+    const long long grid = (long long)r.B * r.Hk;
+    pda_reduce_kernel<<<(unsigned)grid, r.QG * 32, 0, stream>>>(r);
+    return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_LAUNCH;
+}
+
+int device_sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// ------------------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// K|V bytes of one 16-token tile of one KV head.  Dimensions (innermost first):
+//   {128 bytes of a chunk, BS slots, chunks per token-head, Hk heads, NB blocks}
+// with strides {-, Hk*token_head_bytes, 128, token_head_bytes, cache_block_bytes}.  The box
+// {128, 16, chunks, 1, 1} lands as [chunk][token][128 B] in shared memory, 128-byte swizzle.
+static bool encode_kv_map(CUtensorMap* m, const void* cache, const pda_plan_t* p, long long nb) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const int elem = p->kv_dtype == PDA_KV_BF16 ? 2 : 1;
+    const cuuint64_t thb = 2ull * kHeadDim * elem;
+    const cuuint32_t chunks = (cuuint32_t)(thb / 128);
+    cuuint64_t dims[5] = {128, (cuuint64_t)p->kv_block_size, chunks, (cuuint64_t)p->num_kv_heads, (cuuint64_t)nb};
+    cuuint64_t strides[4] = {(cuuint64_t)p->num_kv_heads * thb, 128, thb, (cuuint64_t)p->cache_block_bytes};
+    cuuint32_t box[5] = {128, (cuuint32_t)kTileTokens, chunks, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(cache), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp8 scales of one 16-token tile: fp32 {BS slots, 2 fields, Hk heads, NB blocks} starting at the
+// metadata region; box {16, 2, 1, 1} lands as [field][token].
+static bool encode_scale_map(CUtensorMap* m, const void* cache, const pda_plan_t* p, long long nb) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const char* base = static_cast<const char*>(cache) + p->meta_offset_bytes;
+    cuuint64_t dims[4] = {(cuuint64_t)p->kv_block_size, 2, (cuuint64_t)p->num_kv_heads, (cuuint64_t)nb};
+    cuuint64_t strides[3] = {(cuuint64_t)p->kv_block_size * 4, (cuuint64_t)p->kv_block_size * 8,
+                             (cuuint64_t)p->cache_block_bytes};
+    cuuint32_t box[4] = {(cuuint32_t)kTileTokens, 2, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<char*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------------- plan
+static int compute_plan(const pda_plan_t* in, pda_plan_t* out) {
+    *out = *in;
+    if (in->num_seqs < 0 || in->num_kv_heads < 1 || in->max_blocks_per_seq < 1 || in->tile_groups_per_partition < 0 ||
+        in->max_partitions < 0)
+        return PDA_ERR_INVALID_ARG;
+    if (in->query_group_size != 6 && in->query_group_size != 8 && in->query_group_size != 16)
+        return PDA_ERR_UNSUPPORTED;
+    if (in->kv_block_size != 16 && in->kv_block_size != 32) return PDA_ERR_UNSUPPORTED;
+    if (in->head_dim != kHeadDim) return PDA_ERR_UNSUPPORTED;
+    if (in->kv_dtype != PDA_KV_BF16 && in->kv_dtype != PDA_KV_FP8_E4M3) return PDA_ERR_UNSUPPORTED;
+    if (!std::isfinite(in->softmax_scale)) return PDA_ERR_INVALID_ARG;
+    const long long max_ctx = (long long)in->max_blocks_per_seq * in->kv_block_size;
+    if (max_ctx > (1ll << 30)) return PDA_ERR_INVALID_ARG;   // context lengths are int32
+    long long G = in->tile_groups_per_partition;
+    if (G == 0)
+        G = in->max_partitions <= 0 ? 1
+                                    : (max_ctx + (long long)kTokensPerTileGroup * in->max_partitions - 1) /
+                                          ((long long)kTokensPerTileGroup * in->max_partitions);
+    if (G < 1) G = 1;
+    if (G * kTokensPerTileGroup > (1ll << 30)) return PDA_ERR_INVALID_ARG;
+    const long long W = G * kTokensPerTileGroup;
+    const long long P = (max_ctx + W - 1) / W;
+    // index ranges used by the kernels: units and tiles of a step in int64, grid and rows in int32
+    const long long units = (long long)in->num_seqs * in->num_kv_heads * P;
+    if ((long long)in->num_seqs * in->num_kv_heads > (1ll << 31) - 1 || units * in->query_group_size > (1ll << 40))
+        return PDA_ERR_INVALID_ARG;
+    const int elem = in->kv_dtype == PDA_KV_BF16 ? 2 : 1;
+    const long long data = (long long)in->kv_block_size * in->num_kv_heads * 2 * kHeadDim * elem;
+    const long long meta = in->kv_dtype == PDA_KV_BF16 ? 0 : (long long)in->num_kv_heads * 2 * in->kv_block_size * 4;
+    out->num_partitions = (int)P;
+    out->partition_tokens = (int)W;
+    out->resolved_tile_groups = (int)G;
+    out->resolved_softmax_scale = in->softmax_scale > 0.f ? in->softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
+    out->cache_block_bytes = data + meta;
+    out->meta_offset_bytes = data;
+    out->workspace_bytes = units * in->query_group_size * (kHeadDim * 4 + 8);
+    return PDA_OK;
+}
+
+static bool plan_matches(const pda_plan_t* p) {
+    pda_plan_t chk;
+    if (compute_plan(p, &chk) != PDA_OK) return false;
+    return chk.num_partitions == p->num_partitions && chk.partition_tokens == p->partition_tokens &&
+           chk.resolved_tile_groups == p->resolved_tile_groups &&
+           chk.resolved_softmax_scale == p->resolved_softmax_scale && chk.cache_block_bytes == p->cache_block_bytes &&
+           chk.meta_offset_bytes == p->meta_offset_bytes && chk.workspace_bytes == p->workspace_bytes;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace pda
+
+using namespace pda;
+
+extern "C" {
+
+int pda_plan(pda_plan_t* plan) {
+    if (!plan) return PDA_ERR_INVALID_ARG;
+    pda_plan_t out;
+    const int rc = compute_plan(plan, &out);
+    if (rc == PDA_OK) *plan = out;
+    return rc;
+}
+
+int pda_decode(const pda_plan_t* plan, const void* query, const void* kv_cache, long long num_cache_blocks,
+               const int* block_table, const int* context_lens, float* partial_out, float* exp_sums,
+               float* max_logits, int* err_word, void* stream) {
+    if (!plan || !plan_matches(plan)) return PDA_ERR_INVALID_ARG;
+    if (plan->num_seqs == 0) return PDA_OK;
+    if (!query || !kv_cache || !block_table || !context_lens || !partial_out || !exp_sums || !max_logits)
+        return PDA_ERR_INVALID_ARG;
+    if (num_cache_blocks < 1 || num_cache_blocks > (1ll << 31) - 1) return PDA_ERR_INVALID_ARG;
+    if (!aligned16(query) || !aligned16(kv_cache) || !aligned16(partial_out)) return PDA_ERR_INVALID_ARG;
+    if (((uintptr_t)exp_sums & 3u) || ((uintptr_t)max_logits & 3u) || ((uintptr_t)block_table & 3u) ||
+        ((uintptr_t)context_lens & 3u) || ((uintptr_t)err_word & 3u))
+        return PDA_ERR_INVALID_ARG;
+
+    DecodeArgs a;
+    a.query = static_cast<const uint16_t*>(query);
+    a.block_table = block_table;
+    a.context_lens = context_lens;
+    a.partial_out = partial_out;
+    a.exp_sums = exp_sums;
+    a.max_logits = max_logits;
+    a.err_word = err_word;
+    a.num_cache_blocks = num_cache_blocks;
+    a.B = plan->num_seqs;
+    a.Hk = plan->num_kv_heads;
+    a.QG = plan->query_group_size;
+    a.MB = plan->max_blocks_per_seq;
+    a.BS = plan->kv_block_size;
+    a.P = plan->num_partitions;
+    a.W = plan->partition_tokens;
+    a.qk_scale_log2 = plan->resolved_softmax_scale * 1.4426950408889634f;
+    a.timeout_ns = kDefaultTimeoutNs;
+
+    CUtensorMap kv_map, sc_map;
+    if (!encode_kv_map(&kv_map, kv_cache, plan, num_cache_blocks)) return PDA_ERR_LAUNCH;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (plan->kv_dtype == PDA_KV_BF16) return launch_decode_bf16(a, kv_map, s);
+    if (!encode_scale_map(&sc_map, kv_cache, plan, num_cache_blocks)) return PDA_ERR_LAUNCH;
+    return launch_decode_fp8(a, kv_map, sc_map, s);
+}
+
+int pda_reduce(const pda_plan_t* plan, const int* context_lens, const float* partial_out, const float* exp_sums,
+               const float* max_logits, void* out, int out_dtype, int* err_word, void* stream) {
+    if (!plan || !plan_matches(plan)) return PDA_ERR_INVALID_ARG;
+    if (out_dtype != PDA_OUT_BF16 && out_dtype != PDA_OUT_F32) return PDA_ERR_INVALID_ARG;
+    if (plan->num_seqs == 0) return PDA_OK;
+    if (!context_lens || !partial_out || !exp_sums || !max_logits || !out) return PDA_ERR_INVALID_ARG;
+    if (!aligned16(partial_out) || ((uintptr_t)out & (out_dtype == PDA_OUT_F32 ? 15u : 7u)) ||
+        ((uintptr_t)exp_sums & 3u) || ((uintptr_t)max_logits & 3u) || ((uintptr_t)context_lens & 3u) ||
+        ((uintptr_t)err_word & 3u))
+        return PDA_ERR_INVALID_ARG;
+    ReduceArgs r;
+    r.context_lens = context_lens;
+    r.partial_out = partial_out;
+    r.exp_sums = exp_sums;
+    r.max_logits = max_logits;
+    r.out = out;
+    r.err_word = err_word;
+    r.B = plan->num_seqs;
+    r.Hk = plan->num_kv_heads;
+    r.QG = plan->query_group_size;
+    r.MB = plan->max_blocks_per_seq;
+    r.BS = plan->kv_block_size;
+    r.P = plan->num_partitions;
+    r.W = plan->partition_tokens;
+    r.out_f32 = out_dtype == PDA_OUT_F32;
+    return launch_reduce(r, static_cast<cudaStream_t>(stream));
+}
+
+const char* pda_status_string(int status) {
+    switch (status) {
+        case PDA_OK: return "PDA_OK";
+        case PDA_ERR_INVALID_ARG: return "PDA_ERR_INVALID_ARG";
+        case PDA_ERR_UNSUPPORTED: return "PDA_ERR_UNSUPPORTED";
+        case PDA_ERR_WORKSPACE_TOO_SMALL: return "PDA_ERR_WORKSPACE_TOO_SMALL";
+        case PDA_ERR_LAUNCH: return "PDA_ERR_LAUNCH";
+        case PDA_ERR_NOT_IMPLEMENTED: return "PDA_ERR_NOT_IMPLEMENTED";
+        case PDA_ERR_CUDA: return "PDA_ERR_CUDA";
+        default: return "PDA_ERR_UNKNOWN";
+    }
+}
+
+long long pda_workspace_size(const pda_plan_t* plan) {
+    if (!plan || !plan_matches(plan)) return -1;
+    return plan->workspace_bytes;
+}
+
+int pda_plan_struct_size(void) { return (int)sizeof(pda_plan_t); }
+
+}  // extern "C"

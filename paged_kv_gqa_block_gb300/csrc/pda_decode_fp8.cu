@@ -1,0 +1,14 @@
+// pda_decode_fp8.cu -- instantiation and launch of the partition kernel for an fp8 e4m3 KV cache
+// with one fp32 scale per token per KV head.
+#include "pda_decode.cuh"
+#include "pda_launch.cuh"
+
+namespace pda {
+
+int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, cudaStream_t stream) {
+    // NW = 4 consumer warps, S = 12 stages of 4 KB (+128 B of scales)
+    if (a.QG <= 8) return launch_partition<true, 1, 4, 12>(a, kv_map, sc_map, stream);
+    return launch_partition<true, 2, 4, 12>(a, kv_map, sc_map, stream);
+}
+
+}  // namespace pda

@@ -1,0 +1,50 @@
+// pda_internal.h -- declarations shared by the translation units of libpda (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace pda {
+
+constexpr int kHeadDim = 128;
+constexpr int kTileTokens = 16;          // tokens per MMA tile (TILE_SIZE on the page)
+constexpr int kTokensPerTileGroup = 256; // 16 tiles (KV_COMPUTE_BLOCK on the page)
+constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;   // 1 s per bounded wait
+
+// Arguments of the partition kernel (plain values, passed by value).
+struct DecodeArgs {
+    const uint16_t* query;     // bf16 [B][Hk*QG][D]
+    const int* block_table;    // [B][MB]
+    const int* context_lens;   // [B]
+    float* partial_out;        // [B][Hk][P][QG][D]
+    float* exp_sums;           // [B][Hk][P][QG]
+    float* max_logits;         // [B][Hk][P][QG]
+    int* err_word;             // may be null
+    long long num_cache_blocks;
+    int B, Hk, QG, MB, BS, P, W;
+    float qk_scale_log2;       // softmax_scale * log2(e)
+    unsigned long long timeout_ns;
+};
+
+struct ReduceArgs {
+    const int* context_lens;
+    const float* partial_out;
+    const float* exp_sums;
+    const float* max_logits;
+    void* out;
+    int* err_word;
+    int B, Hk, QG, MB, BS, P, W;
+    int out_f32;
+};
+
+// Launches the partition kernel for one KV format; returns a pda_status value.
+int launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& kv_map, cudaStream_t stream);
+int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
+                      cudaStream_t stream);
+int launch_reduce(const ReduceArgs& r, cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace pda

@@ -1,0 +1,46 @@
+// pda_launch.cuh -- grid sizing and launch of one instance of the partition kernel.
+#pragma once
+
+#include <mutex>
+
+#include "pda.h"
+#include "pda_decode.cuh"
+
+namespace pda {
+
+// Persistent grid: (SMs x resident CTAs per SM), capped by the number of units of the step.
+template <bool FP8, int NT, int NW, int S>
+int launch_partition(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, cudaStream_t stream) {
+    using Cfg = DecodeCfg<FP8, NT, NW, S>;
+    auto kernel = pda_partition_kernel<FP8, NT, NW, S>;
+    static int occ_cache[64] = {0};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PDA_ERR_CUDA;
+    int occ;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (occ_cache[dev] == 0) {
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) !=
+                cudaSuccess)
+                return PDA_ERR_LAUNCH;
+            int o = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, Cfg::kThreads, Cfg::kSmemBytes) !=
+                    cudaSuccess ||
+                o < 1)
+                return PDA_ERR_LAUNCH;
+            occ_cache[dev] = o;
+        }
+        occ = occ_cache[dev];
+    }
+    const int sms = device_sm_count();
+    if (sms <= 0) return PDA_ERR_CUDA;
+    const long long units = (long long)a.B * a.Hk * a.P;
+    long long grid = (long long)sms * occ;
+    if (grid > units) grid = units;
+    if (grid < 1) return PDA_OK;
+    kernel<<<(unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(kv_map, sc_map, a);
+    return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_LAUNCH;
+}
+
+}  // namespace pda

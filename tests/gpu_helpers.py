@@ -1,0 +1,67 @@
+"""Runs the CUDA path (through the C ABI) on generated inputs and hands back numpy arrays."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from paged_kv_gqa_block_gb300 import workloads as wl
+
+SENTINEL_BITS = 0x7FBADBAD   # a NaN payload the kernels never produce
+
+
+def to_device(inp: wl.Inputs, dev="cuda"):
+    return {
+        "query": torch.from_numpy(inp.query.view(np.int16)).to(dev).view(torch.bfloat16),
+        "cache": torch.from_numpy(inp.cache).to(dev),
+        "block_table": torch.from_numpy(np.ascontiguousarray(inp.block_table)).to(dev),
+        "context_lens": torch.from_numpy(np.ascontiguousarray(inp.context_lens)).to(dev),
+    }
+
+
+def plan_for(w: wl.Workload, G=None):
+    import paged_kv_gqa_block_gb300 as pda
+    return pda.plan(w.num_seqs, w.num_kv_heads, w.query_group_size, w.kv_block_size, w.max_blocks_per_seq,
+                    w.tile_groups_per_partition if G is None else G, w.max_partitions, w.kv_dtype, w.softmax_scale)
+
+
+def sentinel_ws(p, dev="cuda"):
+    import paged_kv_gqa_block_gb300 as pda
+    so, ss = pda.partial_shapes(p)
+    mk = lambda s: torch.full(s, SENTINEL_BITS, dtype=torch.int32, device=dev).view(torch.float32)
+    return {"partial_out": mk(so), "exp_sums": mk(ss), "max_logits": mk(ss)}
+
+
+def run_gpu(inp: wl.Inputs, G=None, dev="cuda", d=None):
+    """Partition pass + reduce (fp32 and bf16 outputs).  Returns numpy arrays and the error word."""
+    import paged_kv_gqa_block_gb300 as pda
+    w = inp.workload
+    p = plan_for(w, G)
+    d = d or to_device(inp, dev)
+    ws = sentinel_ws(p, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pda.decode(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"],
+               ws["partial_out"], ws["exp_sums"], ws["max_logits"], err_word=err)
+    out32 = torch.empty((w.num_seqs, w.num_q_heads, 128), dtype=torch.float32, device=dev)
+    out16 = torch.empty((w.num_seqs, w.num_q_heads, 128), dtype=torch.bfloat16, device=dev)
+    pda.reduce(p, d["context_lens"], ws["partial_out"], ws["exp_sums"], ws["max_logits"], out32, err_word=err)
+    pda.reduce(p, d["context_lens"], ws["partial_out"], ws["exp_sums"], ws["max_logits"], out16, err_word=err)
+    torch.cuda.synchronize()
+    return {
+        "plan": p,
+        "out": out32.cpu().numpy().astype(np.float64),
+        "out_bf16": out16.float().cpu().numpy().astype(np.float64),
+        "part_o": ws["partial_out"].cpu().numpy(),
+        "part_m": ws["max_logits"].cpu().numpy(),
+        "part_l": ws["exp_sums"].cpu().numpy(),
+        "err": int(err.item()),
+    }
+
+
+def is_sentinel(a: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float32).view(np.int32) == SENTINEL_BITS
+
+
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half a bf16 ulp at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(ax)) - 8)

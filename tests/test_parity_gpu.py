@@ -1,0 +1,202 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element by element.
+
+Tolerances (the problem's own bar): max-abs 2e-3 on the fp32 output for a bf16 KV cache and
+1e-2 for fp8 e4m3; the bf16 output may differ by that plus half a bf16 ulp of the oracle value.
+Partition partials: o_p within the same tolerance, m_p within 1e-4*max(1,|m|) (fp32 logits),
+l_p within a relative 1e-4.  Block-table walking and partition bookkeeping are checked bit for
+bit: which partials are written (sentinel NaN payload elsewhere), the zero-key count probe
+(m_p = 0 and l_p = token count exactly), the one-hot probe (the output equals one stored V row
+exactly), block relocation and the G independence of short contexts.
+"""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_gqa_block_gb300 import workloads as wl
+from tests import oracle_helpers as oh
+from tests.gpu_helpers import bf16_half_ulp, is_sentinel, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+TOL = {wl.KV_BF16: 2e-3, wl.KV_FP8_E4M3: 1e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def check_against_oracle(inp, res, ref, units=None):
+    w = inp.workload
+    tol = TOL[w.kv_dtype]
+    B, Hk, QG = w.num_seqs, w.num_kv_heads, w.query_group_size
+    W = res["plan"].partition_tokens
+    assert res["err"] == 0
+    ulist = range(B * Hk) if units is None else units
+    for u in ulist:
+        b, h = divmod(int(u), Hk)
+        rows = slice(h * QG, (h + 1) * QG)
+        g, o = res["out"][b, rows], ref["out"][b, rows]
+        assert np.isfinite(g).all()
+        err = np.abs(g - o).max()
+        assert err <= tol, f"unit {u}: out max-abs {err}"
+        gb = res["out_bf16"][b, rows]
+        assert np.all(np.abs(gb - o) <= tol + bf16_half_ulp(o)), f"unit {u}: bf16 out"
+        if ref.get("part_o") is None:
+            continue
+        nv = -(-int(inp.context_lens[b]) // W)
+        P = res["plan"].num_partitions
+        for p in range(P):
+            gm, gl, go = res["part_m"][b, h, p], res["part_l"][b, h, p], res["part_o"][b, h, p]
+            if p < nv:
+                rm, rl, ro = ref["part_m"][b, h, p], ref["part_l"][b, h, p], ref["part_o"][b, h, p]
+                assert not is_sentinel(go).any() and not is_sentinel(gm).any()
+                assert np.abs(go - ro).max() <= tol, f"unit {u} partition {p}: o_p"
+                assert np.all(np.abs(gm - rm) <= 1e-4 * np.maximum(1, np.abs(rm))), f"unit {u} partition {p}: m_p"
+                assert np.all(np.abs(gl - rl) <= 1e-4 * rl), f"unit {u} partition {p}: l_p"
+            else:
+                assert is_sentinel(go).all() and is_sentinel(gm).all() and is_sentinel(gl).all(), \
+                    f"unit {u}: partition {p} >= {nv} was written"
+
+
+SWEEP = [
+    # (kv dtype, QG, BS, G, Hk, context lengths)
+    (wl.KV_BF16, 8, 16, 1, 2, (1, 15, 16, 17, 255, 256, 257, 700)),
+    (wl.KV_BF16, 6, 32, 1, 3, (2, 31, 33, 513, 1000)),
+    (wl.KV_BF16, 16, 16, 2, 2, (1, 511, 512, 513, 1600)),
+    (wl.KV_BF16, 8, 32, 5, 2, (1279, 1280, 1281, 3000)),
+    (wl.KV_BF16, 16, 32, 1, 1, (64, 4097)),
+    (wl.KV_FP8_E4M3, 6, 16, 1, 2, (1, 17, 300, 1100)),
+    (wl.KV_FP8_E4M3, 8, 32, 2, 3, (5, 600, 1500)),
+    (wl.KV_FP8_E4M3, 16, 16, 1, 2, (16, 257, 900)),
+]
+
+
+@pytest.mark.parametrize("kv,QG,BS,G,Hk,ctx", SWEEP)
+def test_sweep_matches_oracle(oracle_mod, kv, QG, BS, G, Hk, ctx):
+    w = wl.small(num_seqs=len(ctx), num_kv_heads=Hk, query_group_size=QG, kv_block_size=BS, ctx=ctx, kv_dtype=kv,
+                 tile_groups_per_partition=G, seed=100 + QG + BS + G, extra_blocks=5)
+    inp = wl.generate(w)
+    res = run_gpu(inp)
+    ref = oh.run_oracle(inp, partials=True, G=G)
+    check_against_oracle(inp, res, ref)
+
+
+def test_key_bias_workload_small(oracle_mod):
+    w = wl.small(num_seqs=3, num_kv_heads=2, query_group_size=16, kv_block_size=32, ctx=(2048, 2100, 3000),
+                 seed=5, k_bias_std=2.0)
+    inp = wl.generate(w)
+    check_against_oracle(inp, run_gpu(inp), oh.run_oracle(inp, partials=True))
+
+
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
+def test_zero_keys_count_probe_is_exact(oracle_mod, kv):
+    ctx = (600, 256, 1)
+    w = wl.small(num_seqs=3, num_kv_heads=2, ctx=ctx, kv_dtype=kv, seed=31)
+    rng = np.random.default_rng(0)
+    K = [np.zeros((c, 2, 128), np.float32) for c in ctx]
+    V = [rng.standard_normal((c, 2, 128)).astype(np.float32) for c in ctx]
+    q = rng.standard_normal((3, w.num_q_heads, 128)).astype(np.float32)
+    inp = oh.build_from_values(w, q, K, V, wl.draw_block_table(w, rng))
+    res = run_gpu(inp)
+    assert res["err"] == 0
+    for b, c in enumerate(ctx):
+        nv = -(-c // 256)
+        for p in range(res["plan"].num_partitions):
+            if p < nv:
+                assert np.all(res["part_m"][b, :, p] == 0.0)
+                assert np.all(res["part_l"][b, :, p] == float(min(256, c - 256 * p)))
+            else:
+                assert is_sentinel(res["part_m"][b, :, p]).all()
+
+
+@pytest.mark.parametrize("ctx,js", [(37, (0, 15, 16, 36)), (700, (0, 255, 256, 511, 699))])
+def test_one_hot_probe_returns_the_stored_row_exactly(oracle_mod, ctx, js):
+    w = wl.small(num_seqs=1, num_kv_heads=2, ctx=(ctx,), seed=32)
+    rng = np.random.default_rng(1)
+    u = rng.standard_normal((2, 128)).astype(np.float32)
+    q = np.repeat(u, 8, axis=0)[None]
+    for j in js:
+        K = np.zeros((ctx, 2, 128), np.float32)
+        K[j] = 150.0 * u / np.linalg.norm(u, axis=1, keepdims=True)   # log2-domain gap > 200: other p are 0
+        V = rng.standard_normal((ctx, 2, 128)).astype(np.float32)
+        inp = oh.build_from_values(w, q, [K], [V], wl.draw_block_table(w, rng))
+        res = run_gpu(inp)
+        vj = oh.stored_values(w, V)[j]
+        out = res["out"][0].reshape(2, 8, 128)
+        for h in range(2):
+            assert np.array_equal(out[h], np.broadcast_to(vj[h], (8, 128))), f"j={j} h={h}"
+
+
+def test_block_relocation_is_bitwise_invariant():
+    w = wl.small(num_seqs=2, num_kv_heads=2, ctx=(900, 77), seed=33, extra_blocks=11)
+    inp = wl.generate(w)
+    a = run_gpu(inp)
+    perm = np.random.default_rng(0).permutation(w.num_cache_blocks)
+    blocks = inp.cache.reshape(w.num_cache_blocks, w.cache_block_bytes)
+    moved = np.empty_like(blocks)
+    moved[perm] = blocks
+    b = run_gpu(wl.Inputs(w, inp.query, moved.reshape(-1), perm[inp.block_table].astype(np.int32), inp.context_lens))
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["part_o"].view(np.int32), b["part_o"].view(np.int32))
+
+
+def test_short_contexts_do_not_depend_on_G():
+    w = wl.small(num_seqs=3, num_kv_heads=2, ctx=(1, 100, 256), seed=34, max_blocks_per_seq=64)
+    inp = wl.generate(w)
+    r1, r2, r5 = run_gpu(inp, G=1), run_gpu(inp, G=2), run_gpu(inp, G=5)
+    assert r1["plan"].num_partitions != r2["plan"].num_partitions
+    assert np.array_equal(r1["out"], r2["out"]) and np.array_equal(r1["out"], r5["out"])
+
+
+def test_repeat_runs_are_bitwise_identical():
+    w = wl.small(num_seqs=4, num_kv_heads=2, ctx=(1000, 3, 513, 2000), seed=35, kv_dtype=wl.KV_FP8_E4M3)
+    inp = wl.generate(w)
+    d = to_device(inp)
+    a, b = run_gpu(inp, d=d), run_gpu(inp, d=d)
+    assert np.array_equal(a["out"], b["out"])
+    for k in ("part_o", "part_m", "part_l"):     # compare bits: unwritten slots hold the NaN sentinel
+        assert np.array_equal(a[k].view(np.int32), b[k].view(np.int32))
+
+
+def test_bad_context_length_sets_error_bit_and_zeroes_that_sequence(oracle_mod):
+    w = wl.small(num_seqs=3, num_kv_heads=2, ctx=(40, 20, 33), seed=36)
+    inp = wl.generate(w)
+    ref = oh.run_oracle(inp)
+    ctx = inp.context_lens.copy()
+    ctx[1] = w.max_blocks_per_seq * w.kv_block_size + 1
+    res = run_gpu(wl.Inputs(w, inp.query, inp.cache, inp.block_table, ctx))
+    assert res["err"] & 1
+    assert np.all(res["out"][1] == 0)
+    for b in (0, 2):
+        assert np.abs(res["out"][b] - ref["out"][b]).max() <= 2e-3
+
+
+def test_bad_block_id_sets_error_bit_without_faulting():
+    w = wl.small(num_seqs=2, num_kv_heads=2, ctx=(40, 20), seed=37)
+    inp = wl.generate(w)
+    bt = inp.block_table.copy()
+    bt[0, 1] = w.num_cache_blocks + 5
+    bt[1, 0] = -3
+    res = run_gpu(wl.Inputs(w, inp.query, inp.cache, bt, inp.context_lens))
+    assert res["err"] & 2
+    assert np.isfinite(res["out"]).all()
+    torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------- full-size workloads
+@pytest.mark.parametrize("name", wl.WORKLOAD_ORDER)
+def test_full_size_workload_sampled_units(oracle_mod, name):
+    w = wl.WORKLOADS[name]
+    inp = wl.generate(w)
+    res = run_gpu(inp)
+    assert res["err"] == 0
+    assert np.isfinite(res["out"]).all()
+    ctx = inp.context_lens
+    Hk = w.num_kv_heads
+    rng = np.random.default_rng(0)
+    picks = {int(np.argmax(ctx)) * Hk, int(np.argmin(ctx)) * Hk + Hk - 1}
+    picks |= set(int(x) for x in rng.choice(w.num_seqs * Hk, size=min(6, w.num_seqs * Hk), replace=False))
+    ref = oh.run_oracle(inp, partials=True, units=sorted(picks))
+    check_against_oracle(inp, res, ref, units=sorted(picks))
