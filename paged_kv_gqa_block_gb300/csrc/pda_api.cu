@@ -15,13 +15,16 @@
 namespace pda {
 
 // ------------------------------------------------------------------------- reduce kernel
-// One CTA per (sequence, KV head); thread (q, d4) combines four output elements of query row q.
-//   M = max_p m_p,  w_p = l_p * e^(m_p - M),  out = sum_p (w_p / sum w) * o_p,  p < ceil(ctx / W).
+// One CTA per (sequence, KV head), one warp per query row q.  Lanes hold the partitions'
+// (m_p, l_p); warp reductions give M = max m_p and sum_p w_p with w_p = l_p * e^(m_p - M);
+// then every lane accumulates four output elements, out = sum_p (w_p / sum w) * o_p, over
+// p < ceil(ctx / W) in partition order with eight partial loads in flight.
 // With one partition w_0 / w_0 == 1 exactly, so the partial is copied bit for bit.
 __global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
+    constexpr float kLog2e = 1.4426950408889634f;
     const int unit = blockIdx.x;
     const int b = unit / r.Hk, h = unit - b * r.Hk;
-    const int q = threadIdx.x >> 5, d4 = (threadIdx.x & 31) << 2;
+    const int q = threadIdx.x >> 5, lane = threadIdx.x & 31, d4 = lane << 2;
     if (q >= r.QG) return;
     int ctx = __ldg(r.context_lens + b);
     if (ctx < 0 || ctx > r.MB * r.BS) {
@@ -30,23 +33,44 @@ __global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
     }
     const int nv = (ctx + r.W - 1) / r.W;
     const long long base = (long long)unit * r.P * r.QG + q;   // index of (unit, p = 0, q)
-    constexpr float kLog2e = 1.4426950408889634f;
     float M = -INFINITY;
-    for (int p = 0; p < nv; ++p) M = fmaxf(M, __ldg(r.max_logits + base + (long long)p * r.QG));
+    for (int p = lane; p < nv; p += 32) M = fmaxf(M, __ldg(r.max_logits + base + (long long)p * r.QG));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
     float wsum = 0.f;
-    for (int p = 0; p < nv; ++p) {
+    for (int p = lane; p < nv; p += 32) {
         const long long i = base + (long long)p * r.QG;
         wsum += __ldg(r.exp_sums + i) * ex2((__ldg(r.max_logits + i) - M) * kLog2e);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, o);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p = 0; p < nv; ++p) {
-        const long long i = base + (long long)p * r.QG;
-        const float coef = __ldg(r.exp_sums + i) * ex2((__ldg(r.max_logits + i) - M) * kLog2e) / wsum;
-        const float4 o = __ldg(reinterpret_cast<const float4*>(r.partial_out + i * kHeadDim + d4));
-        acc.x += coef * o.x;
-        acc.y += coef * o.y;
-        acc.z += coef * o.z;
-        acc.w += coef * o.w;
+    const float* op = r.partial_out + base * kHeadDim + d4;
+    const long long pstride = (long long)r.QG * kHeadDim;
+    for (int c0 = 0; c0 < nv; c0 += 32) {
+        // coefficient of partition c0 + lane
+        float coef = 0.f;
+        if (c0 + lane < nv) {
+            const long long i = base + (long long)(c0 + lane) * r.QG;
+            coef = __ldg(r.exp_sums + i) * ex2((__ldg(r.max_logits + i) - M) * kLog2e) / wsum;
+        }
+        const int cn = min(32, nv - c0);
+        for (int j0 = 0; j0 < cn; j0 += 8) {
+            float4 o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j0 + j < cn) o[j] = __ldg(reinterpret_cast<const float4*>(op + (long long)(c0 + j0 + j) * pstride));
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float cf = __shfl_sync(0xFFFFFFFFu, coef, (j0 + j) & 31);
+                if (j0 + j < cn) {
+                    acc.x += cf * o[j].x;
+                    acc.y += cf * o[j].y;
+                    acc.z += cf * o[j].z;
+                    acc.w += cf * o[j].w;
+                }
+            }
+        }
     }
     const long long orow = (long long)b * r.Hk * r.QG + (long long)h * r.QG + q;
     if (r.out_f32) {
@@ -225,6 +249,7 @@ int pda_decode(const pda_plan_t* plan, const void* query, const void* kv_cache, 
     a.BS = plan->kv_block_size;
     a.P = plan->num_partitions;
     a.W = plan->partition_tokens;
+    a.bs_shift = plan->kv_block_size == 32 ? 5 : 4;
     a.qk_scale_log2 = plan->resolved_softmax_scale * 1.4426950408889634f;
     a.timeout_ns = kDefaultTimeoutNs;
 

@@ -5,9 +5,9 @@
 namespace pda {
 
 int launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& kv_map, cudaStream_t stream) {
-    // NW = 4 consumer warps, S = 8 stages of 8 KB
-    if (a.QG <= 8) return launch_partition<false, 1, 4, 8>(a, kv_map, kv_map, stream);
-    return launch_partition<false, 2, 4, 8>(a, kv_map, kv_map, stream);
+    // one-warp CTAs with a private ring of S = 4 stages of 8 KB
+    if (a.QG <= 8) return launch_partition<false, 1, 4>(a, kv_map, kv_map, stream);
+    return launch_partition<false, 2, 4>(a, kv_map, kv_map, stream);
 }
 
 }  // namespace pda

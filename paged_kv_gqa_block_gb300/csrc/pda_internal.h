@@ -23,6 +23,7 @@ struct DecodeArgs {
     int* err_word;             // may be null
     long long num_cache_blocks;
     int B, Hk, QG, MB, BS, P, W;
+    int bs_shift;              // log2(BS)
     float qk_scale_log2;       // softmax_scale * log2(e)
     unsigned long long timeout_ns;
 };

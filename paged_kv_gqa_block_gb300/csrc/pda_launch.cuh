@@ -8,11 +8,11 @@
 
 namespace pda {
 
-// Persistent grid: (SMs x resident CTAs per SM), capped by the number of units of the step.
-template <bool FP8, int NT, int NW, int S>
+// Persistent grid of one-warp CTAs: (SMs x resident CTAs per SM), capped by the number of units.
+template <bool FP8, int NT, int S>
 int launch_partition(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, cudaStream_t stream) {
-    using Cfg = DecodeCfg<FP8, NT, NW, S>;
-    auto kernel = pda_partition_kernel<FP8, NT, NW, S>;
+    using Cfg = DecodeCfg<FP8, S>;
+    auto kernel = pda_partition_kernel<FP8, NT, S>;
     static int occ_cache[64] = {0};
     static std::mutex mu;
     int dev = 0;
