@@ -15,59 +15,99 @@
 namespace pda {
 
 // ------------------------------------------------------------------------- reduce kernel
-// One CTA per (sequence, KV head), one warp per query row q.  Lanes hold the partitions'
-// (m_p, l_p); warp reductions give M = max m_p and sum_p w_p with w_p = l_p * e^(m_p - M);
-// then every lane accumulates four output elements, out = sum_p (w_p / sum w) * o_p, over
-// p < ceil(ctx / W) in partition order with eight partial loads in flight.
-// With one partition w_0 / w_0 == 1 exactly, so the partial is copied bit for bit.
+// One CTA per (sequence, KV head), one warp per query row q.  Lane j holds (m_p, l_p) of
+// partitions p = j, j+32, ...; warp reductions give M = max m_p and sum_p w_p with
+// w_p = l_p * e^(m_p - M); then every lane accumulates four output elements,
+// out = sum_p (w_p / sum w) * o_p over p < ceil(ctx / W), in partition order, sixteen partial
+// loads in flight.  With one partition w_0 / w_0 == 1 exactly, so the partial is copied bit
+// for bit.  Launched as a programmatic dependent of the partition pass: it waits for that grid
+// before reading the partials.
+constexpr int kReduceRegParts = 4;   // partitions held per lane (up to 128); beyond that (m, l) are reloaded
+
 __global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
     constexpr float kLog2e = 1.4426950408889634f;
     const int unit = blockIdx.x;
     const int b = unit / r.Hk, h = unit - b * r.Hk;
     const int q = threadIdx.x >> 5, lane = threadIdx.x & 31, d4 = lane << 2;
-    if (q >= r.QG) return;
-    int ctx = __ldg(r.context_lens + b);
+    int ctx = __ldg(r.context_lens + b);   // written before the partition pass: no need to wait
     if (ctx < 0 || ctx > r.MB * r.BS) {
         if (h == 0 && threadIdx.x == 0 && r.err_word) atomicOr(r.err_word, PDA_ERRW_BAD_CONTEXT_LEN);
         ctx = 0;
     }
     const int nv = (ctx + r.W - 1) / r.W;
     const long long base = (long long)unit * r.P * r.QG + q;   // index of (unit, p = 0, q)
+    grid_dependency_wait();
+    if (q >= r.QG) return;
+
+    float mr[kReduceRegParts], lr[kReduceRegParts];
     float M = -INFINITY;
-    for (int p = lane; p < nv; p += 32) M = fmaxf(M, __ldg(r.max_logits + base + (long long)p * r.QG));
+#pragma unroll
+    for (int k = 0; k < kReduceRegParts; ++k) {
+        const int p = lane + 32 * k;
+        mr[k] = -INFINITY;
+        lr[k] = 0.f;
+        if (p < nv) {
+            const long long i = base + (long long)p * r.QG;
+            mr[k] = __ldcg(r.max_logits + i);
+            lr[k] = __ldcg(r.exp_sums + i);
+        }
+        M = fmaxf(M, mr[k]);
+    }
+    for (int p = lane + 32 * kReduceRegParts; p < nv; p += 32)
+        M = fmaxf(M, __ldcg(r.max_logits + base + (long long)p * r.QG));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
     float wsum = 0.f;
-    for (int p = lane; p < nv; p += 32) {
+#pragma unroll
+    for (int k = 0; k < kReduceRegParts; ++k) {
+        lr[k] = lr[k] * ex2((mr[k] - M) * kLog2e);   // w_p (0 for p >= nv)
+        wsum += lr[k];
+    }
+    for (int p = lane + 32 * kReduceRegParts; p < nv; p += 32) {
         const long long i = base + (long long)p * r.QG;
-        wsum += __ldg(r.exp_sums + i) * ex2((__ldg(r.max_logits + i) - M) * kLog2e);
+        wsum += __ldcg(r.exp_sums + i) * ex2((__ldcg(r.max_logits + i) - M) * kLog2e);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, o);
+
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float* op = r.partial_out + base * kHeadDim + d4;
-    const long long pstride = (long long)r.QG * kHeadDim;
-    for (int c0 = 0; c0 < nv; c0 += 32) {
-        // coefficient of partition c0 + lane
-        float coef = 0.f;
-        if (c0 + lane < nv) {
-            const long long i = base + (long long)(c0 + lane) * r.QG;
-            coef = __ldg(r.exp_sums + i) * ex2((__ldg(r.max_logits + i) - M) * kLog2e) / wsum;
-        }
-        const int cn = min(32, nv - c0);
-        for (int j0 = 0; j0 < cn; j0 += 8) {
-            float4 o[8];
+    if (nv > 0) {
+        const float* op = r.partial_out + base * kHeadDim + d4;
+        const long long pstride = (long long)r.QG * kHeadDim;
+        for (int c0 = 0; c0 < nv; c0 += 32) {
+            const int k = c0 >> 5;
+            float coef;
+            if (k < kReduceRegParts) {
+                float w = lr[0];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j0 + j < cn) o[j] = __ldg(reinterpret_cast<const float4*>(op + (long long)(c0 + j0 + j) * pstride));
+                for (int kk = 1; kk < kReduceRegParts; ++kk)
+                    if (kk == k) w = lr[kk];
+                coef = w / wsum;
+            } else {
+                const int p = c0 + lane;
+                coef = 0.f;
+                if (p < nv) {
+                    const long long i = base + (long long)p * r.QG;
+                    coef = __ldcg(r.exp_sums + i) * ex2((__ldcg(r.max_logits + i) - M) * kLog2e) / wsum;
+                }
+            }
+            const int cn = min(32, nv - c0);
+            for (int j0 = 0; j0 < cn; j0 += 16) {
+                float4 o[16];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float cf = __shfl_sync(0xFFFFFFFFu, coef, (j0 + j) & 31);
-                if (j0 + j < cn) {
-                    acc.x += cf * o[j].x;
-                    acc.y += cf * o[j].y;
-                    acc.z += cf * o[j].z;
-                    acc.w += cf * o[j].w;
+                for (int j = 0; j < 16; ++j) {   // clamped index: every load is in bounds, extras weigh 0
+                    const int p = min(c0 + j0 + j, nv - 1);
+                    o[j] = __ldcg(reinterpret_cast<const float4*>(op + (long long)p * pstride));
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float cf = __shfl_sync(0xFFFFFFFFu, coef, (j0 + j) & 31);
+                    if (j0 + j < cn) {
+                        acc.x += cf * o[j].x;
+                        acc.y += cf * o[j].y;
+                        acc.z += cf * o[j].z;
+                        acc.w += cf * o[j].w;
+                    }
                 }
             }
         }
@@ -84,9 +124,17 @@ __global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
 }
 
 int launch_reduce(const ReduceArgs& r, cudaStream_t stream) {
-    const long long grid = (long long)r.B * r.Hk;
-    pda_reduce_kernel<<<(unsigned)grid, r.QG * 32, 0, stream>>>(r);
-    return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((long long)r.B * r.Hk));
+    cfg.blockDim = dim3(r.QG * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pda_reduce_kernel, r) == cudaSuccess ? PDA_OK : PDA_ERR_LAUNCH;
 }
 
 int device_sm_count() {

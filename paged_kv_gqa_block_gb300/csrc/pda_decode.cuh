@@ -576,6 +576,8 @@ struct Decode {
             if (FP8) prefetch_tensormap(sc_map);
         }
         __syncwarp();
+        allow_dependent_launch();   // the reduce may be scheduled as soon as CTAs of this grid retire
+        grid_dependency_wait();     // inputs may come from the previous grid on the stream
 
         UnitIt cu;
         long long hi;

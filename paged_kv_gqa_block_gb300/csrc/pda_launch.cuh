@@ -39,8 +39,19 @@ int launch_partition(const DecodeArgs& a, const CUtensorMap& kv_map, const CUten
     long long grid = (long long)sms * occ;
     if (grid > units) grid = units;
     if (grid < 1) return PDA_OK;
-    kernel<<<(unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(kv_map, sc_map, a);
-    return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_LAUNCH;
+    // programmatic dependent launch: the prologue may overlap the tail of the previous grid; the
+    // kernel waits for that grid before it reads any input
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, kv_map, sc_map, a) == cudaSuccess ? PDA_OK : PDA_ERR_LAUNCH;
 }
 
 }  // namespace pda
