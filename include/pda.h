@@ -139,6 +139,30 @@ PDA_API int pda_reduce(const pda_plan_t* plan, const int* context_lens, const fl
                const float* exp_sums, const float* max_logits, void* out, int out_dtype, int* err_word,
                void* stream);
 
+/*
+ * pda_decode_step_noalloc -- pda_decode followed by pda_reduce, for callers that cannot
+ * allocate device memory when they run a step: for example a plugin inside an engine that owns
+ * every byte of device memory, or code that must not call cudaMalloc because it can synchronise
+ * the device.  Such callers can pass inputs and outputs but no partials workspace, so this entry
+ * point keeps the partials in a fixed array inside the library.  The pages describe no such
+ * entry point; it has no counterpart there.
+ *   Arguments are those of pda_decode and pda_reduce without the three partial buffers:
+ *   query, kv_cache, num_cache_blocks, block_table, context_lens as for pda_decode; out and
+ *   out_dtype as for pda_reduce.
+ * The array holds PDA_NOALLOC_SCRATCH_BYTES (64 MiB) on every GPU that loads the library, until
+ * the process exits.  A plan whose partials (B*Hk*P*QG*(D*4 + 8) bytes, each part rounded up to
+ * 256 bytes) do not fit returns PDA_ERR_WORKSPACE_TOO_SMALL and launches nothing.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  The call allocates
+ * nothing and frees nothing.
+ * All calls share the one array and it keeps the last call's contents (nothing in it needs to
+ * start at zero); calls that overlap on the GPU, on any streams, race.
+ */
+#define PDA_NOALLOC_SCRATCH_BYTES (64ll << 20)
+PDA_API int pda_decode_step_noalloc(const pda_plan_t* plan, const void* query, const void* kv_cache,
+                                    long long num_cache_blocks, const int* block_table, const int* context_lens,
+                                    void* out, int out_dtype, int* err_word, void* stream);
+
 /* Human-readable name of a pda_status value (static string; never NULL). */
 PDA_API const char* pda_status_string(int status);
 

@@ -82,6 +82,9 @@ def lib():
             L.pda_status_string.restype = ctypes.c_char_p
             L.pda_workspace_size.argtypes = [P]
             L.pda_workspace_size.restype = ctypes.c_longlong
+            L.pda_decode_step_noalloc.argtypes = [P, _VP, _VP, ctypes.c_longlong, _VP, _VP, _VP, ctypes.c_int, _VP,
+                                                  _VP]
+            L.pda_decode_step_noalloc.restype = ctypes.c_int
             L.pda_plan_struct_size.argtypes = []
             L.pda_plan_struct_size.restype = ctypes.c_int
             if L.pda_plan_struct_size() != ctypes.sizeof(Plan):
@@ -188,3 +191,28 @@ def decode_step(p: Plan, query, kv_cache, num_cache_blocks: int, block_table, co
     reduce(p, context_lens, ws["partial_out"], ws["exp_sums"], ws["max_logits"], out, err_word=err_word,
            stream=stream)
     return out
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def decode_step_noalloc(p: Plan, query, kv_cache, num_cache_blocks: int, block_table, context_lens, out,
+                        err_word=None, stream=None) -> None:
+    """pda_decode_step_noalloc: a whole step with the partials kept inside the library, for callers
+    that cannot allocate a workspace (see include/pda.h).  out [B][Hk*QG][D], bf16 or fp32."""
+    B, Hk, QG, D = p.num_seqs, p.num_kv_heads, p.query_group_size, p.head_dim
+    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    args = (
+        _need(query, "query", (torch.bfloat16, torch.int16, torch.uint16), B * Hk * QG * D * 2),
+        _need(kv_cache, "kv_cache", None, num_cache_blocks * p.cache_block_bytes),
+        ctypes.c_longlong(num_cache_blocks),
+        _need(block_table, "block_table", torch.int32, B * p.max_blocks_per_seq * 4),
+        _need(context_lens, "context_lens", torch.int32, B * 4),
+        _need(out, "out", (torch.float32, torch.bfloat16), B * Hk * QG * D * out.element_size()),
+        ctypes.c_int(out_dtype),
+        None if err_word is None else _need(err_word, "err_word", torch.int32, 4),
+        _stream(stream),
+    )
+    rc = lib().pda_decode_step_noalloc(ctypes.byref(p), *args)
+    if rc != 0:
+        raise PdaError(rc, "pda_decode_step_noalloc")
