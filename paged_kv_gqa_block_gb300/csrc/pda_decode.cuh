@@ -771,8 +771,10 @@ struct Decode {
     }
 };
 
-template <bool FP8, int NT, int S>
-__global__ void __launch_bounds__(32) pda_partition_kernel(const __grid_constant__ CUtensorMap kv_map,
+// MINB: CTAs per SM the register allocation must allow (more resident warps hide the latency of
+// each warp's serial chain of loads, MMAs and shuffles).
+template <bool FP8, int NT, int S, int MINB>
+__global__ void __launch_bounds__(32, MINB) pda_partition_kernel(const __grid_constant__ CUtensorMap kv_map,
                                                           const __grid_constant__ CUtensorMap sc_map,
                                                           const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];

@@ -5,9 +5,9 @@
 namespace pda {
 
 int launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& kv_map, cudaStream_t stream) {
-    // one-warp CTAs with a private ring of S = 4 stages of 8 KB
-    if (a.QG <= 8) return launch_partition<false, 1, 4>(a, kv_map, kv_map, stream);
-    return launch_partition<false, 2, 4>(a, kv_map, kv_map, stream);
+    // one-warp CTAs with a private ring of S = 3 stages of 8 KB, 8 CTAs per SM (QG <= 8)
+    if (a.QG <= 8) return launch_partition<false, 1, 3, 8>(a, kv_map, kv_map, stream);
+    return launch_partition<false, 2, 4, 1>(a, kv_map, kv_map, stream);   // QG = 16: 4 stages, 6 CTAs per SM
 }
 
 }  // namespace pda
