@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=wl.WORKLOAD_ORDER)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="two", choices=["fused", "two"],
+                    help="fused: pda_decode_fused (one launch); two: pda_decode then pda_reduce")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     return ap.parse_args()
@@ -266,10 +268,17 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     B_units = w.num_seqs * w.num_kv_heads
 
+    cnt = pda.counters(p, dev)
+    launches_per_step = 1 if args.path == "fused" else 2
+
     def step():
-        pda.decode(p, q, cache, w.num_cache_blocks, bt, ctx, ws["partial_out"], ws["exp_sums"], ws["max_logits"],
-                   err_word=err, stream=stream)
-        pda.reduce(p, ctx, ws["partial_out"], ws["exp_sums"], ws["max_logits"], out, err_word=err, stream=stream)
+        if args.path == "fused":
+            pda.decode_fused(p, q, cache, w.num_cache_blocks, bt, ctx, ws["partial_out"], ws["exp_sums"],
+                             ws["max_logits"], cnt, out, err_word=err, stream=stream)
+        else:
+            pda.decode(p, q, cache, w.num_cache_blocks, bt, ctx, ws["partial_out"], ws["exp_sums"], ws["max_logits"],
+                       err_word=err, stream=stream)
+            pda.reduce(p, ctx, ws["partial_out"], ws["exp_sums"], ws["max_logits"], out, err_word=err, stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -375,7 +384,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": world * B_units / mean_e2e, "unit": UNIT,
                 "h2d_bytes_per_step": int(qh.numel() * 2 + bth.numel() * 4 + ctxh.numel() * 4),
                 "d2h_bytes_per_step": int(outh.numel() * 2)},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
+        "step_path": "pda_decode_fused (one launch)" if args.path == "fused" else "pda_decode + pda_reduce",
         "decode_launches_timed_separately": dec_steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,

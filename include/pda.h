@@ -140,6 +140,25 @@ PDA_API int pda_reduce(const pda_plan_t* plan, const int* context_lens, const fl
                void* stream);
 
 /*
+ * pda_decode_fused -- one launch for the whole step: the partition pass of pda_decode, and the
+ * reduce of pda_reduce performed inside the same launch by the last partition of each
+ * (sequence, KV head) to finish (the split-reduce pattern of "last arrival sums in order";
+ * nothing waits).  A (sequence, KV head) whose context fits one partition is written to `out`
+ * directly (its partial is not stored).  The combination is the one pda_reduce computes, in
+ * partition order, so results are deterministic and equal pda_decode + pda_reduce's.
+ *   partial_out, exp_sums, max_logits   as for pda_decode (scratch here)
+ *   counters   device int32 [B][Hk]: must be zero before the first call; every completed call
+ *              leaves them zero.  After a call that set PDA_ERRW_PIPELINE_TIMEOUT, zero them
+ *              again before the next call.
+ *   out, out_dtype                      as for pda_reduce
+ * Calls that share counters or partials race if they overlap on the GPU.
+ */
+PDA_API int pda_decode_fused(const pda_plan_t* plan, const void* query, const void* kv_cache,
+                             long long num_cache_blocks, const int* block_table, const int* context_lens,
+                             float* partial_out, float* exp_sums, float* max_logits, int* counters, void* out,
+                             int out_dtype, int* err_word, void* stream);
+
+/*
  * pda_decode_step_noalloc -- pda_decode followed by pda_reduce, for callers that cannot
  * allocate device memory when they run a step: for example a plugin inside an engine that owns
  * every byte of device memory, or code that must not call cudaMalloc because it can synchronise

@@ -82,6 +82,9 @@ def lib():
             L.pda_status_string.restype = ctypes.c_char_p
             L.pda_workspace_size.argtypes = [P]
             L.pda_workspace_size.restype = ctypes.c_longlong
+            L.pda_decode_fused.argtypes = [P, _VP, _VP, ctypes.c_longlong, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                           ctypes.c_int, _VP, _VP]
+            L.pda_decode_fused.restype = ctypes.c_int
             L.pda_decode_step_noalloc.argtypes = [P, _VP, _VP, ctypes.c_longlong, _VP, _VP, _VP, ctypes.c_int, _VP,
                                                   _VP]
             L.pda_decode_step_noalloc.restype = ctypes.c_int
@@ -176,6 +179,36 @@ def reduce(p: Plan, context_lens, partial_out, exp_sums, max_logits, out, err_wo
     rc = lib().pda_reduce(ctypes.byref(p), *args)
     if rc != 0:
         raise PdaError(rc, "pda_reduce")
+
+
+def counters(p: Plan, device):
+    """Arrival counters of the fused step, int32 [B][Hk], zeroed (every completed step leaves them zero)."""
+    return torch.zeros((p.num_seqs, p.num_kv_heads), dtype=torch.int32, device=device)
+
+
+def decode_fused(p: Plan, query, kv_cache, num_cache_blocks: int, block_table, context_lens, partial_out, exp_sums,
+                 max_logits, counters, out, err_word=None, stream=None) -> None:
+    """pda_decode_fused: the partition pass and the reduce in one launch (see include/pda.h)."""
+    B, Hk, QG, D, P = p.num_seqs, p.num_kv_heads, p.query_group_size, p.head_dim, p.num_partitions
+    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    args = (
+        _need(query, "query", (torch.bfloat16, torch.int16, torch.uint16), B * Hk * QG * D * 2),
+        _need(kv_cache, "kv_cache", None, num_cache_blocks * p.cache_block_bytes),
+        ctypes.c_longlong(num_cache_blocks),
+        _need(block_table, "block_table", torch.int32, B * p.max_blocks_per_seq * 4),
+        _need(context_lens, "context_lens", torch.int32, B * 4),
+        _need(partial_out, "partial_out", torch.float32, B * Hk * P * QG * D * 4),
+        _need(exp_sums, "exp_sums", torch.float32, B * Hk * P * QG * 4),
+        _need(max_logits, "max_logits", torch.float32, B * Hk * P * QG * 4),
+        _need(counters, "counters", torch.int32, B * Hk * 4),
+        _need(out, "out", (torch.float32, torch.bfloat16), B * Hk * QG * D * out.element_size()),
+        ctypes.c_int(out_dtype),
+        None if err_word is None else _need(err_word, "err_word", torch.int32, 4),
+        _stream(stream),
+    )
+    rc = lib().pda_decode_fused(ctypes.byref(p), *args)
+    if rc != 0:
+        raise PdaError(rc, "pda_decode_fused")
 
 
 def decode_step(p: Plan, query, kv_cache, num_cache_blocks: int, block_table, context_lens, ws: dict | None = None,

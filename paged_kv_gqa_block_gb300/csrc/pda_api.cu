@@ -25,7 +25,6 @@ namespace pda {
 constexpr int kReduceRegParts = 4;   // partitions held per lane (up to 128); beyond that (m, l) are reloaded
 
 __global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
-    constexpr float kLog2e = 1.4426950408889634f;
     const int unit = blockIdx.x;
     const int b = unit / r.Hk, h = unit - b * r.Hk;
     const int q = threadIdx.x >> 5, lane = threadIdx.x & 31, d4 = lane << 2;
@@ -60,15 +59,15 @@ __global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
     float wsum = 0.f;
 #pragma unroll
     for (int k = 0; k < kReduceRegParts; ++k) {
-        lr[k] = lr[k] * ex2((mr[k] - M) * kLog2e);   // w_p (0 for p >= nv)
-        wsum += lr[k];
+        lr[k] = partition_weight(lr[k], mr[k], M);   // w_p (0 for p >= nv)
+        wsum = __fadd_rn(wsum, lr[k]);
     }
     for (int p = lane + 32 * kReduceRegParts; p < nv; p += 32) {
         const long long i = base + (long long)p * r.QG;
-        wsum += __ldcg(r.exp_sums + i) * ex2((__ldcg(r.max_logits + i) - M) * kLog2e);
+        wsum = __fadd_rn(wsum, partition_weight(__ldcg(r.exp_sums + i), __ldcg(r.max_logits + i), M));
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, o);
+    for (int o = 16; o > 0; o >>= 1) wsum = __fadd_rn(wsum, __shfl_xor_sync(0xFFFFFFFFu, wsum, o));
 
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (nv > 0) {
@@ -82,13 +81,13 @@ __global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
 #pragma unroll
                 for (int kk = 1; kk < kReduceRegParts; ++kk)
                     if (kk == k) w = lr[kk];
-                coef = w / wsum;
+                coef = __fdiv_rn(w, wsum);
             } else {
                 const int p = c0 + lane;
                 coef = 0.f;
                 if (p < nv) {
                     const long long i = base + (long long)p * r.QG;
-                    coef = __ldcg(r.exp_sums + i) * ex2((__ldcg(r.max_logits + i) - M) * kLog2e) / wsum;
+                    coef = __fdiv_rn(partition_weight(__ldcg(r.exp_sums + i), __ldcg(r.max_logits + i), M), wsum);
                 }
             }
             const int cn = min(32, nv - c0);
@@ -103,10 +102,10 @@ __global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
                 for (int j = 0; j < 16; ++j) {
                     const float cf = __shfl_sync(0xFFFFFFFFu, coef, (j0 + j) & 31);
                     if (j0 + j < cn) {
-                        acc.x += cf * o[j].x;
-                        acc.y += cf * o[j].y;
-                        acc.z += cf * o[j].z;
-                        acc.w += cf * o[j].w;
+                        acc.x = fmaf(cf, o[j].x, acc.x);
+                        acc.y = fmaf(cf, o[j].y, acc.y);
+                        acc.z = fmaf(cf, o[j].z, acc.z);
+                        acc.w = fmaf(cf, o[j].w, acc.w);
                     }
                 }
             }
@@ -268,12 +267,22 @@ int pda_plan(pda_plan_t* plan) {
     return rc;
 }
 
-int pda_decode(const pda_plan_t* plan, const void* query, const void* kv_cache, long long num_cache_blocks,
-               const int* block_table, const int* context_lens, float* partial_out, float* exp_sums,
-               float* max_logits, int* err_word, void* stream) {
+}  // extern "C"
+
+namespace pda {
+// The partition pass; with `fused`, the same launch also combines each (sequence, KV head)'s
+// partials into `out` (last-arriving partition merges, counters re-armed to zero).
+static int decode_launch(const pda_plan_t* plan, const void* query, const void* kv_cache, long long num_cache_blocks,
+                         const int* block_table, const int* context_lens, float* partial_out, float* exp_sums,
+                         float* max_logits, int* err_word, void* stream, bool fused, int* counters, void* out,
+                         int out_dtype) {
     if (!plan || !plan_matches(plan)) return PDA_ERR_INVALID_ARG;
+    if (fused && out_dtype != PDA_OUT_BF16 && out_dtype != PDA_OUT_F32) return PDA_ERR_INVALID_ARG;
     if (plan->num_seqs == 0) return PDA_OK;
     if (!query || !kv_cache || !block_table || !context_lens || !partial_out || !exp_sums || !max_logits)
+        return PDA_ERR_INVALID_ARG;
+    if (fused && (!counters || !out || ((uintptr_t)counters & 3u) ||
+                  ((uintptr_t)out & (out_dtype == PDA_OUT_F32 ? 15u : 7u))))
         return PDA_ERR_INVALID_ARG;
     if (num_cache_blocks < 1 || num_cache_blocks > (1ll << 31) - 1) return PDA_ERR_INVALID_ARG;
     if (!aligned16(query) || !aligned16(kv_cache) || !aligned16(partial_out)) return PDA_ERR_INVALID_ARG;
@@ -300,13 +309,33 @@ int pda_decode(const pda_plan_t* plan, const void* query, const void* kv_cache, 
     a.bs_shift = plan->kv_block_size == 32 ? 5 : 4;
     a.qk_scale_log2 = plan->resolved_softmax_scale * 1.4426950408889634f;
     a.timeout_ns = kDefaultTimeoutNs;
+    a.counters = counters;
+    a.out = out;
+    a.out_f32 = out_dtype == PDA_OUT_F32;
 
     CUtensorMap kv_map, sc_map;
     if (!encode_kv_map(&kv_map, kv_cache, plan, num_cache_blocks)) return PDA_ERR_LAUNCH;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (plan->kv_dtype == PDA_KV_BF16) return launch_decode_bf16(a, kv_map, s);
+    if (plan->kv_dtype == PDA_KV_BF16) return launch_decode_bf16(a, kv_map, fused, s);
     if (!encode_scale_map(&sc_map, kv_cache, plan, num_cache_blocks)) return PDA_ERR_LAUNCH;
-    return launch_decode_fp8(a, kv_map, sc_map, s);
+    return launch_decode_fp8(a, kv_map, sc_map, fused, s);
+}
+}  // namespace pda
+
+extern "C" {
+
+int pda_decode(const pda_plan_t* plan, const void* query, const void* kv_cache, long long num_cache_blocks,
+               const int* block_table, const int* context_lens, float* partial_out, float* exp_sums,
+               float* max_logits, int* err_word, void* stream) {
+    return decode_launch(plan, query, kv_cache, num_cache_blocks, block_table, context_lens, partial_out, exp_sums,
+                         max_logits, err_word, stream, false, nullptr, nullptr, PDA_OUT_BF16);
+}
+
+int pda_decode_fused(const pda_plan_t* plan, const void* query, const void* kv_cache, long long num_cache_blocks,
+                     const int* block_table, const int* context_lens, float* partial_out, float* exp_sums,
+                     float* max_logits, int* counters, void* out, int out_dtype, int* err_word, void* stream) {
+    return decode_launch(plan, query, kv_cache, num_cache_blocks, block_table, context_lens, partial_out, exp_sums,
+                         max_logits, err_word, stream, true, counters, out, out_dtype);
 }
 
 int pda_reduce(const pda_plan_t* plan, const int* context_lens, const float* partial_out, const float* exp_sums,

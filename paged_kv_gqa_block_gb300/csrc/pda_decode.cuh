@@ -168,7 +168,7 @@ __device__ inline void find_range(const DecodeArgs& a, UnitIt& u, long long& hi)
 }
 
 // ---------------------------------------------------------------------------------------------
-template <bool FP8, int NT, int S>
+template <bool FP8, int NT, int S, bool FUSED>
 struct Decode {
     using Cfg = DecodeCfg<FP8, S>;
 
@@ -563,6 +563,120 @@ struct Decode {
         }
     }
 
+    // ------------------------------------------------------------------ fused step: output
+    static __device__ __forceinline__ void store_out(const DecodeArgs& a, long long orow, int lane, float4 v) {
+        if (a.out_f32) {
+            *reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * kHeadDim + (lane << 2)) = v;
+        } else {
+            uint2 u;
+            u.x = pack_bf16(v.x, v.y);
+            u.y = pack_bf16(v.z, v.w);
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow * kHeadDim + (lane << 2)) = u;
+        }
+    }
+    // The partitions' partials of one (sequence, head), combined in partition order exactly as the
+    // reduce kernel combines them: M = max m_p, w_p = l_p e^(m_p - M), out = sum (w_p / sum w) o_p.
+    // Up to 64 partitions: one round of loads brings (m_p, l_p) of every row, weights and sums
+    // stay in registers, and each row's partials are read sixteen at a time.
+    static __device__ void merge_unit(const DecodeArgs& a, const UnitIt& u, int lane) {
+        constexpr int QR = NT * 8;
+        const int nv = u.nv;
+        const long long base = (long long)(u.b * a.Hk + u.h) * a.P * a.QG;   // (p = 0, q = 0)
+        const long long orow0 = (long long)u.b * a.Hk * a.QG + (long long)u.h * a.QG;
+        const long long pstride = (long long)a.QG * kHeadDim;
+        if (nv > 64) {
+            merge_unit_general(a, u, lane);
+            return;
+        }
+        float coef[2][QR];
+        {
+            float mv[2][QR], lv[2][QR];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int p = lane + 32 * c;
+#pragma unroll
+                for (int q = 0; q < QR; ++q) {
+                    const bool ok = p < nv && q < a.QG;
+                    mv[c][q] = ok ? __ldcg(a.max_logits + base + (long long)p * a.QG + q) : -INFINITY;
+                    lv[c][q] = ok ? __ldcg(a.exp_sums + base + (long long)p * a.QG + q) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < QR; ++q) {
+                float M = fmaxf(mv[0][q], mv[1][q]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+                const float w0 = partition_weight(lv[0][q], mv[0][q], M);
+                const float w1 = partition_weight(lv[1][q], mv[1][q], M);
+                float wsum = __fadd_rn(w0, w1);   // the reduce kernel's order: chunk 0 then chunk 1
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) wsum = __fadd_rn(wsum, __shfl_xor_sync(kFull, wsum, o));
+                coef[0][q] = __fdiv_rn(w0, wsum);
+                coef[1][q] = __fdiv_rn(w1, wsum);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < QR; ++q) {
+            if (q >= a.QG) break;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float* op = a.partial_out + (base + q) * kHeadDim + (lane << 2);
+            for (int p0 = 0; p0 < nv; p0 += 16) {
+                float4 o[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)   // clamped index: every load is in bounds, extras weigh 0
+                    o[j] = __ldcg(reinterpret_cast<const float4*>(op + (long long)min(p0 + j, nv - 1) * pstride));
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int p = p0 + j;
+                    const float cf = __shfl_sync(kFull, (p & 32) ? coef[1][q] : coef[0][q], p & 31);
+                    if (p < nv) {
+                        acc.x = fmaf(cf, o[j].x, acc.x);
+                        acc.y = fmaf(cf, o[j].y, acc.y);
+                        acc.z = fmaf(cf, o[j].z, acc.z);
+                        acc.w = fmaf(cf, o[j].w, acc.w);
+                    }
+                }
+            }
+            store_out(a, orow0 + q, lane, acc);
+        }
+    }
+    // Any number of partitions, one row at a time.
+    static __device__ __noinline__ void merge_unit_general(const DecodeArgs& a, const UnitIt& u, int lane) {
+        const int nv = u.nv;
+        const long long base = (long long)(u.b * a.Hk + u.h) * a.P * a.QG;
+        const long long orow0 = (long long)u.b * a.Hk * a.QG + (long long)u.h * a.QG;
+        const long long pstride = (long long)a.QG * kHeadDim;
+        for (int q = 0; q < a.QG; ++q) {
+            float M = -INFINITY;
+            for (int p = lane; p < nv; p += 32) M = fmaxf(M, __ldcg(a.max_logits + base + (long long)p * a.QG + q));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+            float wsum = 0.f;
+            for (int p = lane; p < nv; p += 32) {
+                const long long i = base + (long long)p * a.QG + q;
+                wsum = __fadd_rn(wsum, partition_weight(__ldcg(a.exp_sums + i), __ldcg(a.max_logits + i), M));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wsum = __fadd_rn(wsum, __shfl_xor_sync(kFull, wsum, o));
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float* op = a.partial_out + (base + q) * kHeadDim + (lane << 2);
+            for (int p = 0; p < nv; ++p) {
+                float coef = 0.f;
+                if (lane == (p & 31)) {
+                    const long long i = base + (long long)p * a.QG + q;
+                    coef = __fdiv_rn(partition_weight(__ldcg(a.exp_sums + i), __ldcg(a.max_logits + i), M), wsum);
+                }
+                const float cf = __shfl_sync(kFull, coef, p & 31);
+                const float4 o = __ldcg(reinterpret_cast<const float4*>(op + (long long)p * pstride));
+                acc.x = fmaf(cf, o.x, acc.x);
+                acc.y = fmaf(cf, o.y, acc.y);
+                acc.z = fmaf(cf, o.z, acc.z);
+                acc.w = fmaf(cf, o.w, acc.w);
+            }
+            store_out(a, orow0 + q, lane, acc);
+        }
+    }
+
     // ------------------------------------------------------------------ the warp
     static __device__ void run(const DecodeArgs& a, const CUtensorMap* kv_map, const CUtensorMap* sc_map,
                                uint8_t* smem) {
@@ -732,13 +846,21 @@ struct Decode {
                 }
                 __syncwarp();
                 const int rows = min(kPass * 8, a.QG - n0 * 8);
-                for (int q = 0; q < rows; ++q) {
-                    const float4 v = *reinterpret_cast<const float4*>(stg + q * kHeadDim + ((lane ^ (q & 6)) << 2));
-                    *reinterpret_cast<float4*>(a.partial_out + (row0 + n0 * 8 + q) * kHeadDim + (lane << 2)) = v;
+                if (FUSED && cu.nv == 1) {   // the partial is the output (the reduce would copy it)
+                    const long long orow = (long long)cu.b * a.Hk * a.QG + (long long)cu.h * a.QG + n0 * 8;
+                    for (int q = 0; q < rows; ++q) {
+                        const float4 v = *reinterpret_cast<const float4*>(stg + q * kHeadDim + ((lane ^ (q & 6)) << 2));
+                        store_out(a, orow + q, lane, v);
+                    }
+                } else {
+                    for (int q = 0; q < rows; ++q) {
+                        const float4 v = *reinterpret_cast<const float4*>(stg + q * kHeadDim + ((lane ^ (q & 6)) << 2));
+                        *reinterpret_cast<float4*>(a.partial_out + (row0 + n0 * 8 + q) * kHeadDim + (lane << 2)) = v;
+                    }
                 }
                 __syncwarp();
             }
-            if (gid == 0) {
+            if (gid == 0 && !(FUSED && cu.nv == 1)) {
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -753,6 +875,21 @@ struct Decode {
             // the staging stage goes back to the feed (its generic writes precede the copy)
             fence_proxy_async_shared();
             if (feed_one(a, hi, kv_map, sc_map, sbase, bar0 + 8 * stage, stage, f, lane)) ++issued;
+            if constexpr (FUSED) {
+                if (cu.nv > 1) {
+                    // publish this partial; the last partition of the (sequence, head) to arrive merges all
+                    __threadfence();
+                    __syncwarp();
+                    int old = 0;
+                    if (lane == 0) old = atomicAdd(a.counters + (long long)cu.b * a.Hk + cu.h, 1);
+                    old = __shfl_sync(kFull, old, 0);
+                    if (old == cu.nv - 1) {
+                        __threadfence();
+                        merge_unit(a, cu, lane);
+                        if (lane == 0) a.counters[(long long)cu.b * a.Hk + cu.h] = 0;   // re-armed for the next step
+                    }
+                }
+            }
             if (!has_next) break;
             cu = nx;
         }
@@ -773,13 +910,13 @@ struct Decode {
 
 // MINB: CTAs per SM the register allocation must allow (more resident warps hide the latency of
 // each warp's serial chain of loads, MMAs and shuffles).
-template <bool FP8, int NT, int S, int MINB>
+template <bool FP8, int NT, int S, int MINB, bool FUSED>
 __global__ void __launch_bounds__(32, MINB) pda_partition_kernel(const __grid_constant__ CUtensorMap kv_map,
                                                           const __grid_constant__ CUtensorMap sc_map,
                                                           const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Decode<FP8, NT, S>::run(a, &kv_map, &sc_map, smem);
+    Decode<FP8, NT, S, FUSED>::run(a, &kv_map, &sc_map, smem);
 }
 
 }  // namespace pda

@@ -5,11 +5,16 @@
 
 namespace pda {
 
-int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, cudaStream_t stream) {
+int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, bool fused,
+                      cudaStream_t stream) {
     // one-warp CTAs with a private ring of S = 4 stages of 4 KB (+128 B of scales); 12 CTAs per SM
     // for QG <= 8 (168 registers), 8 for QG = 16 (which needs the full register budget)
-    if (a.QG <= 8) return launch_partition<true, 1, 4, 12>(a, kv_map, sc_map, stream);
-    return launch_partition<true, 2, 4, 8>(a, kv_map, sc_map, stream);
+    if (fused) {
+        if (a.QG <= 8) return launch_partition<true, 1, 4, 12, true>(a, kv_map, sc_map, stream);
+        return launch_partition<true, 2, 4, 8, true>(a, kv_map, sc_map, stream);
+    }
+    if (a.QG <= 8) return launch_partition<true, 1, 4, 12, false>(a, kv_map, sc_map, stream);
+    return launch_partition<true, 2, 4, 8, false>(a, kv_map, sc_map, stream);
 }
 
 }  // namespace pda

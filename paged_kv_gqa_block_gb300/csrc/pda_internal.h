@@ -26,6 +26,10 @@ struct DecodeArgs {
     int bs_shift;              // log2(BS)
     float qk_scale_log2;       // softmax_scale * log2(e)
     unsigned long long timeout_ns;
+    // fused step only: per-(sequence, KV head) arrival counters and the final output
+    int* counters;             // [B][Hk], zero before the launch, left zero after it
+    void* out;                 // [B][Hk*QG][D] bf16 or fp32
+    int out_f32;
 };
 
 struct ReduceArgs {
@@ -40,8 +44,8 @@ struct ReduceArgs {
 };
 
 // Launches the partition kernel for one KV format; returns a pda_status value.
-int launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& kv_map, cudaStream_t stream);
-int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
+int launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& kv_map, bool fused, cudaStream_t stream);
+int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, bool fused,
                       cudaStream_t stream);
 int launch_reduce(const ReduceArgs& r, cudaStream_t stream);
 

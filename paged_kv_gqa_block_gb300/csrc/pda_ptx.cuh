@@ -146,6 +146,13 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint
         : "r"(w));
 }
 
+// Weight of one partition in the reduce, w_p = l_p * 2^((m_p - M) * log2 e), with every rounding
+// pinned (no contraction) so that the reduce kernel and the fused step's in-kernel merge give
+// the same bits.
+__device__ __forceinline__ float partition_weight(float l_p, float m_p, float M) {
+    return __fmul_rn(l_p, ex2(__fmul_rn(__fsub_rn(m_p, M), 1.4426950408889634f)));
+}
+
 // Orders this thread's earlier generic-proxy shared-memory accesses before later async-proxy
 // (TMA) accesses to the same memory.
 __device__ __forceinline__ void fence_proxy_async_shared() {

@@ -1,0 +1,76 @@
+"""The fused step (partition pass and reduce in one launch) against the oracle and against the
+two-launch path, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_gqa_block_gb300 import workloads as wl
+from tests import oracle_helpers as oh
+from tests.gpu_helpers import bf16_half_ulp, plan_for, to_device
+
+pytestmark = pytest.mark.gpu
+
+TOL = {wl.KV_BF16: 2e-3, wl.KV_FP8_E4M3: 1e-2}
+
+
+@pytest.fixture(scope="module")
+def pda():
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_gqa_block_gb300 as pda
+    return pda
+
+
+def run_both(pda, inp, G=None, repeats=2):
+    w = inp.workload
+    p = plan_for(w, G)
+    d = to_device(inp)
+    shape = (w.num_seqs, w.num_q_heads, 128)
+    two = torch.empty(shape, dtype=torch.float32, device="cuda")
+    pda.decode_step(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"], out=two)
+    ws = pda.workspace(p, "cuda")
+    cnt = pda.counters(p, "cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(repeats):
+        for dt in (torch.float32, torch.bfloat16):
+            o = torch.full(shape, float("nan"), dtype=dt, device="cuda")
+            pda.decode_fused(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"],
+                             ws["partial_out"], ws["exp_sums"], ws["max_logits"], cnt, o, err_word=err)
+            outs.append(o)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert int(cnt.abs().sum().item()) == 0, "counters must be left at zero"
+    return two.cpu().numpy().astype(np.float64), [o.float().cpu().numpy().astype(np.float64) for o in outs]
+
+
+CASES = [
+    (wl.KV_BF16, 8, 16, 1, 2, (1, 15, 256, 257, 700, 4000)),
+    (wl.KV_BF16, 16, 32, 2, 2, (33, 600, 2049)),
+    (wl.KV_BF16, 6, 32, 5, 3, (1281, 40, 3000)),
+    (wl.KV_FP8_E4M3, 6, 16, 1, 2, (1, 300, 1100, 5000)),
+    (wl.KV_FP8_E4M3, 16, 16, 1, 2, (16, 900)),
+]
+
+
+@pytest.mark.parametrize("kv,QG,BS,G,Hk,ctx", CASES)
+def test_fused_matches_oracle_and_the_two_launch_path(oracle_mod, pda, kv, QG, BS, G, Hk, ctx):
+    w = wl.small(num_seqs=len(ctx), num_kv_heads=Hk, query_group_size=QG, kv_block_size=BS, ctx=ctx, kv_dtype=kv,
+                 tile_groups_per_partition=G, seed=200 + QG + BS + G, extra_blocks=5)
+    inp = wl.generate(w)
+    two, fused = run_both(pda, inp)
+    ref = oh.run_oracle(inp, G=G)["out"]
+    tol = TOL[kv]
+    for k, o in enumerate(fused):
+        if k % 2 == 0:   # fp32 outputs: same combination, same order as the two-launch path
+            assert np.array_equal(o, two), "fused and two-launch results differ"
+            assert np.abs(o - ref).max() <= tol
+        else:            # bf16 outputs
+            assert np.all(np.abs(o - ref) <= tol + bf16_half_ulp(ref))
+
+
+@pytest.mark.parametrize("name", ["b8_hk8_qg8_bs16_ctx1-4096", "b64_hk8_qg6_bs16_fp8_lognormal2048"])
+def test_fused_full_size_equals_two_launch(pda, name):
+    inp = wl.generate(wl.WORKLOADS[name])
+    two, fused = run_both(pda, inp, repeats=1)
+    assert np.array_equal(fused[0], two)
