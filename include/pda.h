@@ -57,7 +57,8 @@ enum { PDA_OUT_BF16 = 0, PDA_OUT_F32 = 1 };
 enum {
     PDA_ERRW_BAD_CONTEXT_LEN = 1,   /* context_lens[b] < 0 or > max_blocks_per_seq*kv_block_size */
     PDA_ERRW_BAD_BLOCK_ID = 2,      /* a block-table entry used by the context is outside [0, NB) */
-    PDA_ERRW_PIPELINE_TIMEOUT = 4   /* a bounded wait inside the kernel gave up */
+    PDA_ERRW_PIPELINE_TIMEOUT = 4,  /* a bounded wait inside the kernel gave up */
+    PDA_ERRW_BAD_POSITION = 8       /* pda_append_kv: a position >= max_blocks_per_seq*kv_block_size */
 };
 
 /*
@@ -138,6 +139,27 @@ PDA_API int pda_decode(const pda_plan_t* plan, const void* query, const void* kv
 PDA_API int pda_reduce(const pda_plan_t* plan, const int* context_lens, const float* partial_out,
                const float* exp_sums, const float* max_logits, void* out, int out_dtype, int* err_word,
                void* stream);
+
+/*
+ * pda_append_kv -- the write side of the same cache: stores K and V of one new token for every
+ * sequence b with positions[b] >= 0, at token index positions[b]: cache block
+ * block_table[b][pos / BS], slot pos % BS (the paged slot formula of the KV insert on the
+ * DeepSeek attention-front page: block = slot // block_size, offset = slot % block_size, and a
+ * negative slot means no write).
+ *   k_new, v_new  device, bf16 [B][Hk][D], 8-byte aligned
+ *   kv_cache      device, the cache pda_decode reads (16-byte aligned)
+ *   positions     device, int32 [B]
+ * bf16 caches store the values as given.  fp8 caches store, per (token, KV head) and separately
+ * for K and V, scale = absmax / 448 in fp32 (1 when the row is all zero) in the metadata region
+ * and codes e4m3(x / scale), both divisions correctly rounded in fp32, the conversion rounding to
+ * nearest even and saturating at +-448.
+ * Data errors (nothing is written for that sequence): a position >= MB*BS sets
+ * PDA_ERRW_BAD_POSITION, a block id outside [0, NB) sets PDA_ERRW_BAD_BLOCK_ID.
+ * Two sequences whose table entries name the same block and slot race.
+ */
+PDA_API int pda_append_kv(const pda_plan_t* plan, const void* k_new, const void* v_new, void* kv_cache,
+                          long long num_cache_blocks, const int* block_table, const int* positions, int* err_word,
+                          void* stream);
 
 /*
  * pda_decode_fused -- one launch for the whole step: the partition pass of pda_decode, and the

@@ -17,6 +17,8 @@ Contents
   * ``decode()``           the attention itself (see ``pda_oracle.c`` for the definition and the
                            passages it follows), optionally with per-partition partials.
   * ``e4m3_to_float64()``  the OCP FP8 E4M3 decode written from the format definition.
+  * ``e4m3_encode()``      its encode: nearest finite code by brute force, ties to even, saturating.
+  * ``append_kv()``        the write side: one new token per sequence into the paged cache.
 
 Parity of every function here is pinned by ``tests/test_oracle_pins.py`` against closed forms,
 invariants, brute force, library routines and the page's worked sizing example.
@@ -69,6 +71,10 @@ def load_library(path: str):
         ctypes.c_int64] + [ctypes.c_void_p] * 4
     lib.oracle_e4m3_to_double.restype = ctypes.c_double
     lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.oracle_append_kv.restype = ctypes.c_int
+    lib.oracle_append_kv.argtypes = [ctypes.POINTER(_Problem)] + [ctypes.c_void_p] * 5
     return lib
 
 
@@ -199,3 +205,31 @@ def decode(problem: Problem, query: np.ndarray, cache: np.ndarray, block_table: 
             raise ValueError({-1: "context length outside [0, MB*BS]", -2: "block id outside the pool",
                               -3: "out of memory"}.get(rc, f"oracle error {rc}"))
     return {"out": out, "part_o": po, "part_m": pm, "part_l": plv, "threads": len(chunks)}
+
+
+def e4m3_encode(values, lib=None) -> np.ndarray:
+    lib = lib or _load()
+    v = np.asarray(values, dtype=np.float32)
+    return np.array([lib.oracle_e4m3_encode(float(x)) for x in v.ravel()], dtype=np.uint8).reshape(v.shape)
+
+
+def append_kv(problem: Problem, cache: np.ndarray, k_new: np.ndarray, v_new: np.ndarray, block_table: np.ndarray,
+              positions: np.ndarray, lib=None) -> np.ndarray:
+    """Returns a copy of ``cache`` with one token per sequence appended (see pda_oracle.c).
+    k_new, v_new: uint16 bf16 bits [B][Hk][D]; positions: int32 [B] (negative: no write)."""
+    lib = lib or _load()
+    pr = problem
+    lay = cache_layout(pr.num_kv_heads, pr.kv_block_size, pr.head_dim, pr.kv_dtype)
+    pl = plan(pr.max_blocks_per_seq, pr.kv_block_size, pr.tile_groups_per_partition)
+    cp = _Problem(pr.num_seqs, pr.num_kv_heads, 8, pr.head_dim, pr.kv_block_size, pr.max_blocks_per_seq, pr.kv_dtype,
+                  pl["W"], pl["P"], pr.num_cache_blocks, lay["cache_block_bytes"], lay["meta_offset_bytes"], pr.scale)
+    out = np.array(cache, dtype=np.uint8, copy=True)
+    kn = np.ascontiguousarray(k_new, dtype=np.uint16)
+    vn = np.ascontiguousarray(v_new, dtype=np.uint16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    rc = lib.oracle_append_kv(ctypes.byref(cp), kn.ctypes.data, vn.ctypes.data, out.ctypes.data, bt.ctypes.data,
+                              pos.ctypes.data)
+    if rc != 0:
+        raise ValueError({-1: "position outside [0, MB*BS)", -2: "block id outside the pool"}.get(rc, f"oracle error {rc}"))
+    return out

@@ -209,3 +209,83 @@ int oracle_decode_units(const oracle_problem* pr, const uint16_t* query, const u
     }
     return ORACLE_OK;
 }
+
+/* ---------------------------------------------------------------------------------------------
+ * The write side of the same cache: appending one token per sequence.
+ *
+ * OCP FP8 E4M3 encoding by brute force over the format's finite values: the code of |x| is the
+ * finite non-negative code nearest to |x| (ties to the code with an even mantissa, i.e. round to
+ * nearest even), values above the largest finite value (448) saturate to it, and the sign of x
+ * is copied into the sign bit.  NaN input gives the NaN code.
+ */
+uint8_t oracle_e4m3_encode(float x) {
+    if (x != x) return 0x7F;
+    const double ax = fabs((double)x);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {               /* 0x7F is NaN */
+        const double v = oracle_e4m3_to_double((uint8_t)c);
+        const double d = fabs(v - ax);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(best | (signbit(x) ? 0x80 : 0));
+}
+
+/*
+ * Writes K and V of one new token for every sequence b with positions[b] >= 0, at token index
+ * positions[b]: cache block block_table[b][pos / BS], slot pos % BS (the paged slot formula
+ * block = slot // block_size, offset = slot % block_size of the KV insert on the DeepSeek
+ * attention-front page; a negative slot means "no write" there too).
+ * bf16: the values are stored as given.  fp8: per (token, KV head) and separately for K and V,
+ * scale = absmax / 448 in fp32 (1 when the row is all zero), code = e4m3(x / scale) with x / scale
+ * rounded to fp32, and the scale is stored in the metadata region [kv_head][K,V][slot].
+ *   k_new, v_new  bf16 bits [B][Hk][D];  positions int32 [B].
+ * Returns ORACLE_OK, ORACLE_BAD_CTX for a position >= MB*BS, ORACLE_BAD_BLOCK for a block id
+ * outside the pool (nothing is written for that sequence in either case).
+ */
+int oracle_append_kv(const oracle_problem* pr, const uint16_t* k_new, const uint16_t* v_new, uint8_t* cache,
+                     const int32_t* block_table, const int32_t* positions) {
+    const int64_t Hk = pr->num_kv_heads, D = pr->head_dim, BS = pr->kv_block_size, MB = pr->max_blocks_per_seq;
+    int rc = ORACLE_OK;
+    for (int64_t b = 0; b < pr->num_seqs; ++b) {
+        const int64_t pos = positions[b];
+        if (pos < 0) continue;
+        if (pos >= MB * BS) { rc = ORACLE_BAD_CTX; continue; }
+        const int64_t blk = block_table[b * MB + pos / BS], slot = pos % BS;
+        if (blk < 0 || blk >= pr->num_cache_blocks) { rc = ORACLE_BAD_BLOCK; continue; }
+        uint8_t* block = cache + blk * pr->cache_block_bytes;
+        for (int64_t h = 0; h < Hk; ++h) {
+            for (int which = 0; which < 2; ++which) {
+                const uint16_t* src = (which == 0 ? k_new : v_new) + (b * Hk + h) * D;
+                if (pr->kv_dtype == 0) {
+                    uint8_t* row = block + (slot * Hk + h) * 2 * D * 2 + (int64_t)which * D * 2;
+                    for (int64_t d = 0; d < D; ++d) {
+                        row[2 * d] = (uint8_t)(src[d] & 0xFF);
+                        row[2 * d + 1] = (uint8_t)(src[d] >> 8);
+                    }
+                } else {
+                    uint8_t* row = block + (slot * Hk + h) * 2 * D + (int64_t)which * D;
+                    float amax = 0.0f;
+                    for (int64_t d = 0; d < D; ++d) {
+                        const float v = (float)bf16_bits_to_double(src[d]);
+                        amax = fmaxf(amax, fabsf(v));
+                    }
+                    const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+                    for (int64_t d = 0; d < D; ++d) {
+                        const float v = (float)bf16_bits_to_double(src[d]);
+                        const float y = v / scale;
+                        row[d] = oracle_e4m3_encode(y);
+                    }
+                    uint8_t* sp = block + pr->meta_offset_bytes + ((h * 2 + which) * BS + slot) * 4;
+                    uint32_t u;
+                    memcpy(&u, &scale, 4);
+                    sp[0] = (uint8_t)u; sp[1] = (uint8_t)(u >> 8); sp[2] = (uint8_t)(u >> 16); sp[3] = (uint8_t)(u >> 24);
+                }
+            }
+        }
+    }
+    return rc;
+}

@@ -29,6 +29,7 @@ OUT_F32 = 1
 ERRW_BAD_CONTEXT_LEN = 1
 ERRW_BAD_BLOCK_ID = 2
 ERRW_PIPELINE_TIMEOUT = 4
+ERRW_BAD_POSITION = 8
 HEAD_DIM = 128
 
 STATUS = {0: "PDA_OK", -1: "PDA_ERR_INVALID_ARG", -2: "PDA_ERR_UNSUPPORTED", -3: "PDA_ERR_WORKSPACE_TOO_SMALL",
@@ -82,6 +83,8 @@ def lib():
             L.pda_status_string.restype = ctypes.c_char_p
             L.pda_workspace_size.argtypes = [P]
             L.pda_workspace_size.restype = ctypes.c_longlong
+            L.pda_append_kv.argtypes = [P, _VP, _VP, _VP, ctypes.c_longlong, _VP, _VP, _VP, _VP]
+            L.pda_append_kv.restype = ctypes.c_int
             L.pda_decode_fused.argtypes = [P, _VP, _VP, ctypes.c_longlong, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                            ctypes.c_int, _VP, _VP]
             L.pda_decode_fused.restype = ctypes.c_int
@@ -179,6 +182,26 @@ def reduce(p: Plan, context_lens, partial_out, exp_sums, max_logits, out, err_wo
     rc = lib().pda_reduce(ctypes.byref(p), *args)
     if rc != 0:
         raise PdaError(rc, "pda_reduce")
+
+
+def append_kv(p: Plan, k_new, v_new, kv_cache, num_cache_blocks: int, block_table, positions, err_word=None,
+              stream=None) -> None:
+    """pda_append_kv: writes one new token per sequence into the paged cache (see include/pda.h).
+    k_new, v_new: bf16 [B][Hk][D]; positions: int32 [B] (negative: no write)."""
+    B, Hk, D = p.num_seqs, p.num_kv_heads, p.head_dim
+    args = (
+        _need(k_new, "k_new", (torch.bfloat16, torch.int16, torch.uint16), B * Hk * D * 2),
+        _need(v_new, "v_new", (torch.bfloat16, torch.int16, torch.uint16), B * Hk * D * 2),
+        _need(kv_cache, "kv_cache", None, num_cache_blocks * p.cache_block_bytes),
+        ctypes.c_longlong(num_cache_blocks),
+        _need(block_table, "block_table", torch.int32, B * p.max_blocks_per_seq * 4),
+        _need(positions, "positions", torch.int32, B * 4),
+        None if err_word is None else _need(err_word, "err_word", torch.int32, 4),
+        _stream(stream),
+    )
+    rc = lib().pda_append_kv(ctypes.byref(p), *args)
+    if rc != 0:
+        raise PdaError(rc, "pda_append_kv")
 
 
 def counters(p: Plan, device):
