@@ -55,6 +55,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="two", choices=["fused", "two"],
                     help="fused: pda_decode_fused (one launch); two: pda_decode then pda_reduce")
+    ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     return ap.parse_args()
@@ -265,6 +266,8 @@ def run_ours(args, rank, world, local_rank):
             flush_buf.zero_()       # evicts everything from L2 ...
             clean_buf.sum()         # ... and leaves it holding clean lines of another buffer
     flush = _Flush()
+    if args.graph:      # graphs are captured on a non-default stream: run everything on one
+        torch.cuda.set_stream(torch.cuda.Stream(dev))
     stream = torch.cuda.current_stream(dev)
     B_units = w.num_seqs * w.num_kv_heads
 
@@ -284,6 +287,19 @@ def run_ours(args, rank, world, local_rank):
         flush.zero_()
         step()
     torch.cuda.synchronize()
+    if args.graph:      # capture one step; the timed loops replay it
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        torch.cuda.synchronize()
+        step_direct = step
+
+        def step():
+            graph.replay()
+        for _ in range(3):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())}")
 
@@ -385,7 +401,8 @@ def run_ours(args, rank, world, local_rank):
                 "h2d_bytes_per_step": int(qh.numel() * 2 + bth.numel() * 4 + ctxh.numel() * 4),
                 "d2h_bytes_per_step": int(outh.numel() * 2)},
         "gpu_launches": launches_per_step * args.steps,
-        "step_path": "pda_decode_fused (one launch)" if args.path == "fused" else "pda_decode + pda_reduce",
+        "step_path": ("pda_decode_fused (one launch)" if args.path == "fused" else "pda_decode + pda_reduce") +
+                     (", replayed from a CUDA graph" if args.graph else ""),
         "decode_launches_timed_separately": dec_steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
