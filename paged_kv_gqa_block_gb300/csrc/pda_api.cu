@@ -15,22 +15,36 @@
 namespace pda {
 
 // ------------------------------------------------------------------------- reduce kernel
-// One CTA per (sequence, KV head), one warp per query row q.  Lane j holds (m_p, l_p) of
-// partitions p = j, j+32, ...; warp reductions give M = max m_p and sum_p w_p with
-// w_p = l_p * e^(m_p - M); then every lane accumulates four output elements,
+// One CTA per (sequence, KV head, group of up to 8 query rows), one warp per query row q.
+// Lane j holds (m_p, l_p) of partitions p = j, j+32, ...; warp reductions give M = max m_p and
+// sum_p w_p with w_p = l_p * e^(m_p - M); then every lane accumulates four output elements,
 // out = sum_p (w_p / sum w) * o_p over p < ceil(ctx / W), in partition order, sixteen partial
-// loads in flight.  With one partition w_0 / w_0 == 1 exactly, so the partial is copied bit
-// for bit.  Launched as a programmatic dependent of the partition pass: it waits for that grid
-// before reading the partials.
-constexpr int kReduceRegParts = 4;   // partitions held per lane (up to 128); beyond that (m, l) are reloaded
+// loads in flight.  The first sixteen partials are requested together with (m_p, l_p), so a
+// row of up to sixteen partitions costs one round trip to L2.  With one partition
+// w_0 / w_0 == 1 exactly, so the partial is copied bit for bit.  Launched as a programmatic
+// dependent of the partition pass: it waits for that grid before reading the partials.
+constexpr int kReduceRegParts = 2;   // partitions held per lane (up to 64); beyond that (m, l) are reloaded
+constexpr int kReduceRows = 8;       // query rows (warps) per CTA
+constexpr int kReduceBatch = 16;     // partial loads in flight per lane
 
-__global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
-    const int unit = blockIdx.x;
+__device__ __forceinline__ void load_partial_batch(const float* op, int pstride, int p0, int nv,
+                                                   float4 (&o)[kReduceBatch]) {
+    const float4* o4 = reinterpret_cast<const float4*>(op);
+    const int s4 = pstride >> 2;   // float4s between partitions (QG * D / 4)
+#pragma unroll
+    for (int j = 0; j < kReduceBatch; ++j)   // clamped index: every load is in bounds, extras weigh 0
+        o[j] = __ldcg(o4 + (long long)min(p0 + j, nv - 1) * s4);
+}
+
+__global__ void __launch_bounds__(kReduceRows * 32) pda_reduce_kernel(const ReduceArgs r) {
+    const int groups = (r.QG + kReduceRows - 1) / kReduceRows;
+    const int unit = blockIdx.x / groups;
+    const int q = (blockIdx.x - unit * groups) * kReduceRows + (threadIdx.x >> 5);
     const int b = unit / r.Hk, h = unit - b * r.Hk;
-    const int q = threadIdx.x >> 5, lane = threadIdx.x & 31, d4 = lane << 2;
+    const int lane = threadIdx.x & 31, d4 = lane << 2;
     int ctx = __ldg(r.context_lens + b);   // written before the partition pass: no need to wait
     if (ctx < 0 || ctx > r.MB * r.BS) {
-        if (h == 0 && threadIdx.x == 0 && r.err_word) atomicOr(r.err_word, PDA_ERRW_BAD_CONTEXT_LEN);
+        if (h == 0 && q == 0 && lane == 0 && r.err_word) atomicOr(r.err_word, PDA_ERRW_BAD_CONTEXT_LEN);
         ctx = 0;
     }
     const int nv = (ctx + r.W - 1) / r.W;
@@ -38,8 +52,9 @@ __global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
     grid_dependency_wait();
     if (q >= r.QG) return;
 
+    const float* op = r.partial_out + base * kHeadDim + d4;
+    const int pstride = r.QG * kHeadDim;
     float mr[kReduceRegParts], lr[kReduceRegParts];
-    float M = -INFINITY;
 #pragma unroll
     for (int k = 0; k < kReduceRegParts; ++k) {
         const int p = lane + 32 * k;
@@ -50,12 +65,16 @@ __global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
             mr[k] = __ldcg(r.max_logits + i);
             lr[k] = __ldcg(r.exp_sums + i);
         }
-        M = fmaxf(M, mr[k]);
     }
+    float4 o[kReduceBatch];
+    if (nv > 0) load_partial_batch(op, pstride, 0, nv, o);   // in flight with (m, l)
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kReduceRegParts; ++k) M = fmaxf(M, mr[k]);
     for (int p = lane + 32 * kReduceRegParts; p < nv; p += 32)
         M = fmaxf(M, __ldcg(r.max_logits + base + (long long)p * r.QG));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    for (int o_ = 16; o_ > 0; o_ >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o_));
     float wsum = 0.f;
 #pragma unroll
     for (int k = 0; k < kReduceRegParts; ++k) {
@@ -67,46 +86,37 @@ __global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
         wsum = __fadd_rn(wsum, partition_weight(__ldcg(r.exp_sums + i), __ldcg(r.max_logits + i), M));
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wsum = __fadd_rn(wsum, __shfl_xor_sync(0xFFFFFFFFu, wsum, o));
+    for (int o_ = 16; o_ > 0; o_ >>= 1) wsum = __fadd_rn(wsum, __shfl_xor_sync(0xFFFFFFFFu, wsum, o_));
 
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (nv > 0) {
-        const float* op = r.partial_out + base * kHeadDim + d4;
-        const long long pstride = (long long)r.QG * kHeadDim;
-        for (int c0 = 0; c0 < nv; c0 += 32) {
-            const int k = c0 >> 5;
-            float coef;
-            if (k < kReduceRegParts) {
-                float w = lr[0];
+    for (int c0 = 0; c0 < nv; c0 += 32) {
+        const int k = c0 >> 5;
+        float coef;
+        if (k < kReduceRegParts) {
+            float w = lr[0];
 #pragma unroll
-                for (int kk = 1; kk < kReduceRegParts; ++kk)
-                    if (kk == k) w = lr[kk];
-                coef = __fdiv_rn(w, wsum);
-            } else {
-                const int p = c0 + lane;
-                coef = 0.f;
-                if (p < nv) {
-                    const long long i = base + (long long)p * r.QG;
-                    coef = __fdiv_rn(partition_weight(__ldcg(r.exp_sums + i), __ldcg(r.max_logits + i), M), wsum);
-                }
+            for (int kk = 1; kk < kReduceRegParts; ++kk)
+                if (kk == k) w = lr[kk];
+            coef = __fdiv_rn(w, wsum);
+        } else {
+            const int p = c0 + lane;
+            coef = 0.f;
+            if (p < nv) {
+                const long long i = base + (long long)p * r.QG;
+                coef = __fdiv_rn(partition_weight(__ldcg(r.exp_sums + i), __ldcg(r.max_logits + i), M), wsum);
             }
-            const int cn = min(32, nv - c0);
-            for (int j0 = 0; j0 < cn; j0 += 16) {
-                float4 o[16];
+        }
+        const int cn = min(32, nv - c0);
+        for (int j0 = 0; j0 < cn; j0 += kReduceBatch) {
+            if (c0 + j0 > 0) load_partial_batch(op, pstride, c0 + j0, nv, o);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {   // clamped index: every load is in bounds, extras weigh 0
-                    const int p = min(c0 + j0 + j, nv - 1);
-                    o[j] = __ldcg(reinterpret_cast<const float4*>(op + (long long)p * pstride));
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float cf = __shfl_sync(0xFFFFFFFFu, coef, (j0 + j) & 31);
-                    if (j0 + j < cn) {
-                        acc.x = fmaf(cf, o[j].x, acc.x);
-                        acc.y = fmaf(cf, o[j].y, acc.y);
-                        acc.z = fmaf(cf, o[j].z, acc.z);
-                        acc.w = fmaf(cf, o[j].w, acc.w);
-                    }
+            for (int j = 0; j < kReduceBatch; ++j) {
+                const float cf = __shfl_sync(0xFFFFFFFFu, coef, (j0 + j) & 31);
+                if (j0 + j < cn) {
+                    acc.x = fmaf(cf, o[j].x, acc.x);
+                    acc.y = fmaf(cf, o[j].y, acc.y);
+                    acc.z = fmaf(cf, o[j].z, acc.z);
+                    acc.w = fmaf(cf, o[j].w, acc.w);
                 }
             }
         }
@@ -123,9 +133,12 @@ __global__ void __launch_bounds__(512) pda_reduce_kernel(const ReduceArgs r) {
 }
 
 int launch_reduce(const ReduceArgs& r, cudaStream_t stream) {
+    const int groups = (r.QG + kReduceRows - 1) / kReduceRows;
+    const long long ctas = (long long)r.B * r.Hk * groups;
+    const int threads = min(r.QG, kReduceRows) * 32;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((long long)r.B * r.Hk));
-    cfg.blockDim = dim3(r.QG * 32);
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -185,6 +185,7 @@ struct Decode {
         UnitIt nu;     // next chunk
         int ne0, nent;
         bool nvalid;
+        uint64_t policy;   // L2 policy of the tile copies (read once: evict first)
     };
 
     static __device__ __forceinline__ int n_entries(const DecodeArgs& a, const UnitIt& u) {
@@ -217,6 +218,7 @@ struct Decode {
         f.ent = f.valid ? load_entry(a, f.u, 0, lane) : 0;
         f.pf = false;
         f.nvalid = false;
+        f.policy = l2_policy_evict_first();
     }
     // Issues the next tile into `stage` (whole warp; lane 0 issues).  Returns false when the
     // warp's range has no more tiles.
@@ -229,9 +231,11 @@ struct Decode {
         if (lane == 0) {
             const int slot0 = (f.t & ((1 << ts) - 1)) * kTileTokens;
             mbar_arrive_expect_tx(bar, Cfg::kTileBytes + Cfg::kScaleBytes);
-            tma_load_5d(sbase + Cfg::kOffStages + stage * Cfg::kTileBytes, kv_map, bar, 0, slot0, 0, f.u.h, phys);
+            tma_load_5d(sbase + Cfg::kOffStages + stage * Cfg::kTileBytes, kv_map, bar, 0, slot0, 0, f.u.h, phys,
+                        f.policy);
             if constexpr (FP8)
-                tma_load_4d(sbase + Cfg::kOffScales + stage * Cfg::kScaleBytes, sc_map, bar, slot0, 0, f.u.h, phys);
+                tma_load_4d(sbase + Cfg::kOffScales + stage * Cfg::kScaleBytes, sc_map, bar, slot0, 0, f.u.h, phys,
+                            f.policy);
             if ((phys < 0 || (long long)phys >= a.num_cache_blocks) && a.err_word)
                 atomicOr(a.err_word, PDA_ERRW_BAD_BLOCK_ID);
         }
