@@ -65,6 +65,23 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(dist, values, device="cpu"):
+    """Replicas: every rank times its own copy of the step and the slowest rank sets the time.
+    Returns the element-wise maximum of `values` over all ranks (the values themselves when
+    there is no process group)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def replica_throughput(world: int, units_per_rank: int, seconds_per_step: float) -> float:
+    """Units processed per second by all ranks together (each rank runs the whole step)."""
+    return world * units_per_rank / seconds_per_step
+
+
 def kv_bytes_per_token_head(w: wl.Workload) -> int:
     return 2 * w.head_dim * w.elem_bytes + (8 if w.kv_dtype == wl.KV_FP8_E4M3 else 0)
 
@@ -336,9 +353,7 @@ def run_ours(args, rank, world, local_rank):
     t_dec = [a.elapsed_time(b) * 1e-3 for a, b in evd]
     mean_step, mean_dec = sum(t_step) / len(t_step), sum(t_dec) / len(t_dec)
     if dist:
-        tt = torch.tensor([mean_step, mean_dec], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        mean_step, mean_dec = float(tt[0]), float(tt[1])
+        mean_step, mean_dec = max_over_ranks(dist, [mean_step, mean_dec], dev)
 
     # ---- end to end through the public API with host buffers
     qh = torch.from_numpy(inp.query.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -362,9 +377,7 @@ def run_ours(args, rank, world, local_rank):
             e2e.append(a.elapsed_time(b) * 1e-3)
     mean_e2e = sum(e2e) / len(e2e)
     if dist:
-        tt = torch.tensor([mean_e2e], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        mean_e2e = float(tt[0])
+        mean_e2e, = max_over_ranks(dist, [mean_e2e], dev)
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())}")
@@ -379,7 +392,7 @@ def run_ours(args, rank, world, local_rank):
     achieved = ab["decode"] / mean_dec / 1e9
     kv_gbs = ab["kv"] / mean_step / 1e9
     res = {
-        "metric": METRIC, "value": world * B_units / mean_step, "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": replica_throughput(world, B_units, mean_step), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.kv_dtype == wl.KV_BF16 else "fp8_e4m3",
@@ -397,7 +410,7 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": committed_traffic(w.name), "kernel": "pda_partition_kernel",
                      "algorithmic_bytes_per_launch": ab["decode"],
                      "peak_source": "measured" if peaks else "fallback"},
-        "e2e": {"value": world * B_units / mean_e2e, "unit": UNIT,
+        "e2e": {"value": replica_throughput(world, B_units, mean_e2e), "unit": UNIT,
                 "h2d_bytes_per_step": int(qh.numel() * 2 + bth.numel() * 4 + ctxh.numel() * 4),
                 "d2h_bytes_per_step": int(outh.numel() * 2)},
         "gpu_launches": launches_per_step * args.steps,
