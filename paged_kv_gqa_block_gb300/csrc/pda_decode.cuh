@@ -96,36 +96,83 @@ __device__ __forceinline__ void it_advance(UnitIt& u, const DecodeArgs& a) {
     }
 }
 
-// One warp: count the tiles of the step, split them evenly over all warps of the grid and
-// return this warp's first unit (u.b == B when it has none) and the end of its tile range.
-// Sets the data-error bit for out-of-range context lengths (block 0 only).
+// One warp: count the tiles and the units of the step and choose this warp's work.  With no
+// more units than warps, warp k takes unit k alone (nothing is gained by pairing units: the
+// longest warp would hold two).  Otherwise the tiles are split evenly over the warps and a warp
+// takes the units whose first tile falls in its share.  Returns the warp's first unit
+// (u.b == B when it has none) and the end of its tile range.  Sets the data-error bit for
+// out-of-range context lengths (block 0 only).
 __device__ inline void find_range(const DecodeArgs& a, UnitIt& u, long long& hi) {
     const int lane = threadIdx.x & 31;
     const int max_ctx = a.MB * a.BS;
     const int per = (a.B + 31) >> 5;
     const int b0 = min(a.B, lane * per), b1 = min(a.B, b0 + per);
-    long long mine = 0;
+    long long mine = 0, mine_u = 0;   // tiles and units of this lane's sequences
     bool bad = false;
     for (int b = b0; b < b1; ++b) {
         const int raw = __ldg(a.context_lens + b);
         if (raw < 0 || raw > max_ctx) bad = true;
-        mine += (long long)a.Hk * ((sanitize_ctx(raw, max_ctx) + 15) >> 4);
+        const int c = sanitize_ctx(raw, max_ctx);
+        mine += (long long)a.Hk * ((c + 15) >> 4);
+        mine_u += (long long)a.Hk * ((c + a.W - 1) / a.W);
     }
     if (bad && blockIdx.x == 0 && a.err_word) atomicOr(a.err_word, PDA_ERRW_BAD_CONTEXT_LEN);
-    long long incl = mine;
+    long long incl = mine, incl_u = mine_u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const long long n = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += n;
+        const long long nu = __shfl_up_sync(kFull, incl_u, o);
+        if (lane >= o) {
+            incl += n;
+            incl_u += nu;
+        }
     }
     const long long total = __shfl_sync(kFull, incl, 31);
-    const long long excl = incl - mine;
-    const long long lo = (long long)blockIdx.x * total / gridDim.x;
-    hi = ((long long)blockIdx.x + 1) * total / gridDim.x;
-    // the lane whose sequences contain tile `lo` finds the first unit starting at or after it
+    const long long units = __shfl_sync(kFull, incl_u, 31);
+    const long long excl = incl - mine, excl_u = incl_u - mine_u;
     int fb = a.B, fh = 0, fp = 0;
     long long fs = 0;
     int found = 0;
+    if (units <= gridDim.x) {
+        // unit k = blockIdx.x, found by the lane whose sequences hold it
+        const long long k = blockIdx.x;
+        hi = 0;
+        if (mine_u > 0 && excl_u <= k && k < excl_u + mine_u) {
+            long long pos = excl, pos_u = excl_u;
+            for (int b = b0; b < b1; ++b) {
+                const int c = sanitize_ctx(__ldg(a.context_lens + b), max_ctx);
+                const long long th = (c + 15) >> 4;
+                const long long nv = (c + a.W - 1) / a.W;
+                if (k < pos_u + a.Hk * nv) {
+                    const long long r = k - pos_u;
+                    fb = b;
+                    fh = (int)(r / nv);
+                    fp = (int)(r - fh * nv);
+                    fs = pos + fh * th + (long long)fp * (a.W >> 4);
+                    found = 1;
+                    break;
+                }
+                pos += a.Hk * th;
+                pos_u += a.Hk * nv;
+            }
+        }
+        const unsigned m = __ballot_sync(kFull, found);
+        const int src = m ? __ffs(m) - 1 : 0;
+        u.b = m ? __shfl_sync(kFull, fb, src) : a.B;
+        u.h = __shfl_sync(kFull, fh, src);
+        u.p = __shfl_sync(kFull, fp, src);
+        u.start = __shfl_sync(kFull, fs, src);
+        u.ctx = 0;
+        u.nv = 0;
+        if (u.b < a.B) {
+            it_settle(u, a);
+            hi = u.start + unit_tiles(u, a.W);
+        }
+        return;
+    }
+    const long long lo = (long long)blockIdx.x * total / gridDim.x;
+    hi = ((long long)blockIdx.x + 1) * total / gridDim.x;
+    // the lane whose sequences contain tile `lo` finds the first unit starting at or after it
     if (mine > 0 && excl <= lo && lo < excl + mine) {
         long long pos = excl;
         for (int b = b0; b < b1; ++b) {

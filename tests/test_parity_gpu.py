@@ -84,6 +84,18 @@ def test_sweep_matches_oracle(oracle_mod, kv, QG, BS, G, Hk, ctx):
     check_against_oracle(inp, res, ref)
 
 
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
+def test_more_units_than_warps(oracle_mod, kv):
+    # 2600 to 3000 (sequence, KV head, partition) units: more than the persistent grid has warps,
+    # so warps take tile-balanced runs of several units (fewer units give one unit per warp)
+    rng = np.random.default_rng(9)
+    ctx = tuple(int(c) for c in rng.integers(257, 1025, size=120))
+    w = wl.small(num_seqs=120, num_kv_heads=8, query_group_size=6, kv_block_size=16, ctx=ctx, kv_dtype=kv, seed=41)
+    inp = wl.generate(w)
+    assert sum(8 * -(-c // 256) for c in ctx) > 2432
+    check_against_oracle(inp, run_gpu(inp), oh.run_oracle(inp, partials=True))
+
+
 def test_key_bias_workload_small(oracle_mod):
     w = wl.small(num_seqs=3, num_kv_heads=2, query_group_size=16, kv_block_size=32, ctx=(2048, 2100, 3000),
                  seed=5, k_bias_std=2.0)
