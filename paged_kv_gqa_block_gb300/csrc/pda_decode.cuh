@@ -227,6 +227,7 @@ struct Decode {
         int e0;        // first block-table entry of the current chunk (relative to the unit)
         int ent;       // this lane's entry of the current chunk
         int t;         // next tile of the unit to issue
+        int nt;        // tiles of the unit
         bool valid;
         bool pf;       // the next chunk has been looked up and its entries requested
         UnitIt nu;     // next chunk
@@ -262,6 +263,7 @@ struct Decode {
         f.e0 = 0;
         f.t = 0;
         f.valid = first.b < a.B && first.start < hi;
+        f.nt = f.valid ? unit_tiles(first, a.W) : 0;
         f.ent = f.valid ? load_entry(a, f.u, 0, lane) : 0;
         f.pf = false;
         f.nvalid = false;
@@ -287,15 +289,17 @@ struct Decode {
                 atomicOr(a.err_word, PDA_ERRW_BAD_BLOCK_ID);
         }
         ++f.t;
-        const int nt = unit_tiles(f.u, a.W);
-        if (f.t == nt || (f.t >> ts) - f.e0 >= 32) {     // move to the next chunk
+        if (f.t == f.nt || (f.t >> ts) - f.e0 >= 32) {     // move to the next chunk
             if (!f.pf) prefetch_next(a, hi, f, lane);
-            const bool same_unit = f.t < nt;
+            const bool same_unit = f.t < f.nt;
             f.u = f.nu;
             f.e0 = f.ne0;
             f.ent = f.nent;
             f.valid = f.nvalid;
-            if (!same_unit) f.t = 0;
+            if (!same_unit) {
+                f.t = 0;
+                f.nt = unit_tiles(f.u, a.W);
+            }
             f.pf = false;
             if (f.valid) prefetch_next(a, hi, f, lane);   // one chunk ahead
         }
@@ -537,7 +541,7 @@ struct Decode {
         fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 8));
         fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 16));
         if (!(fv > 0.f)) fv = 1.f;
-        const float rF = 1.f / fv;
+        const float rF = rcp_approx(fv);   // acc and F move together: only their product matters
         const float ratio = F * rF;   // acc holds true_acc / F; rebase it on this step's factor
         F = fv;
 #pragma unroll
@@ -760,7 +764,8 @@ struct Decode {
             if (feed_one(a, hi, kv_map, sc_map, sbase, bar0 + 8 * s, s, f, lane)) ++issued;
         if (f.valid && !f.pf) prefetch_next(a, hi, f, lane);
 
-        long long i = 0;                     // tiles consumed
+        int cs = 0;                          // next stage to consume and its barrier phase
+        uint32_t cph = 0;
         bool ok = true;
         while (ok) {
             // ---- unit start: Q fragments, next unit's Q in flight
@@ -818,9 +823,11 @@ struct Decode {
             int stage = 0;
             for (int t = 0; t < nt;) {
                 const bool two = t + 1 < nt;
-                const int s0 = (int)(i % S), s1 = (int)((i + 1) % S);
-                if (!mbar_wait(bar0 + 8 * s0, (uint32_t)((i / S) & 1), a.timeout_ns) ||
-                    (two && !mbar_wait(bar0 + 8 * s1, (uint32_t)(((i + 1) / S) & 1), a.timeout_ns))) {
+                const int s0 = cs;
+                const uint32_t ph0 = cph;
+                const int s1 = s0 + 1 == S ? 0 : s0 + 1;
+                const uint32_t ph1 = s0 + 1 == S ? cph ^ 1u : cph;
+                if (!mbar_wait(bar0 + 8 * s0, ph0, a.timeout_ns) || (two && !mbar_wait(bar0 + 8 * s1, ph1, a.timeout_ns))) {
                     ok = false;
                     break;
                 }
@@ -860,7 +867,8 @@ struct Decode {
                 } else if (two) {
                     if (feed_one(a, hi, kv_map, sc_map, sbase, bar0 + 8 * s0, s0, f, lane)) ++issued;
                 }
-                i += used;
+                cs = two ? (s1 + 1 == S ? 0 : s1 + 1) : s1;
+                cph = two ? (s1 + 1 == S ? ph1 ^ 1u : ph1) : ph1;
             }
             if (!ok) break;
 

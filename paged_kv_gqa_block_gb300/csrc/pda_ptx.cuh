@@ -129,6 +129,12 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 }
 
 // ------------------------------------------------------------------ arithmetic helpers
+// Hardware reciprocal (rcp.approx, flush-to-zero).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 // Hardware base-2 exponential (ex2.approx, flush-to-zero); ex2(-inf) = +0.
 __device__ __forceinline__ float ex2(float x) {
     float y;
