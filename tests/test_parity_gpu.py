@@ -96,6 +96,20 @@ def test_more_units_than_warps(oracle_mod, kv):
     check_against_oracle(inp, run_gpu(inp), oh.run_oracle(inp, partials=True))
 
 
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
+def test_one_unit_per_warp(oracle_mod, kv):
+    # room for 16 x 8 x 16 = 2048 partitions (more than the grid's warps) but short contexts
+    # give at most 16 x 8 x 3 = 384 non-empty ones: each warp takes one whole unit
+    rng = np.random.default_rng(11)
+    ctx = tuple(int(c) for c in rng.integers(1, 769, size=16))
+    w = wl.small(num_seqs=16, num_kv_heads=8, query_group_size=8, kv_block_size=16, ctx=ctx, kv_dtype=kv, seed=42,
+                 max_blocks_per_seq=256)
+    inp = wl.generate(w)
+    res = run_gpu(inp)
+    assert res["plan"].num_partitions == 16
+    check_against_oracle(inp, res, oh.run_oracle(inp, partials=True))
+
+
 def test_key_bias_workload_small(oracle_mod):
     w = wl.small(num_seqs=3, num_kv_heads=2, query_group_size=16, kv_block_size=32, ctx=(2048, 2100, 3000),
                  seed=5, k_bias_std=2.0)
