@@ -79,6 +79,12 @@ typedef struct pda_plan_t {
     int max_partitions;            /* cap used when G == 0 (0 = no cap, i.e. G = 1)              */
     int kv_dtype;                  /* PDA_KV_BF16 or PDA_KV_FP8_E4M3                              */
     float softmax_scale;           /* <= 0 selects 1/sqrt(head_dim)                                */
+    int wait_timeout_ns;           /* limit of each bounded wait inside pda_decode's kernel, in
+                                      nanoseconds; 0 = 1 s.  A wait that gives up sets
+                                      PDA_ERRW_PIPELINE_TIMEOUT.  Copies already in flight are
+                                      always waited for (up to 1 s) before a warp leaves.  No
+                                      counterpart on the pages; small values exist for testing
+                                      the timeout path.                                          */
     /* ---- outputs of pda_plan ---- */
     int num_partitions;            /* P = ceil(MB*BS / W)                                          */
     int partition_tokens;          /* W = G * 256                                                 */

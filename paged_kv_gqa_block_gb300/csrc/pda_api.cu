@@ -219,7 +219,7 @@ static bool encode_scale_map(CUtensorMap* m, const void* cache, const pda_plan_t
 static int compute_plan(const pda_plan_t* in, pda_plan_t* out) {
     *out = *in;
     if (in->num_seqs < 0 || in->num_kv_heads < 1 || in->max_blocks_per_seq < 1 || in->tile_groups_per_partition < 0 ||
-        in->max_partitions < 0)
+        in->max_partitions < 0 || in->wait_timeout_ns < 0)
         return PDA_ERR_INVALID_ARG;
     if (in->query_group_size != 6 && in->query_group_size != 8 && in->query_group_size != 16)
         return PDA_ERR_UNSUPPORTED;
@@ -321,7 +321,7 @@ static int decode_launch(const pda_plan_t* plan, const void* query, const void* 
     a.W = plan->partition_tokens;
     a.bs_shift = plan->kv_block_size == 32 ? 5 : 4;
     a.qk_scale_log2 = plan->resolved_softmax_scale * 1.4426950408889634f;
-    a.timeout_ns = kDefaultTimeoutNs;
+    a.timeout_ns = plan->wait_timeout_ns > 0 ? (unsigned long long)plan->wait_timeout_ns : kDefaultTimeoutNs;
     a.counters = counters;
     a.out = out;
     a.out_f32 = out_dtype == PDA_OUT_F32;

@@ -955,11 +955,12 @@ struct Decode {
         if (!ok) {
             if (lane == 0) {
                 if (a.err_word) atomicOr(a.err_word, PDA_ERRW_PIPELINE_TIMEOUT);
-                // wait (bounded) for the last copy issued into every stage
+                // wait (bounded, by the default limit whatever the plan asked for) for the last copy
+                // issued into every stage: no copy may land in this CTA's memory after it leaves
                 for (int s = 0; s < S; ++s) {
                     if (issued <= s) continue;
                     const long long j = s + ((issued - 1 - s) / S) * S;
-                    (void)mbar_wait(bar0 + 8 * s, (uint32_t)((j / S) & 1), a.timeout_ns);
+                    (void)mbar_wait(bar0 + 8 * s, (uint32_t)((j / S) & 1), kDefaultTimeoutNs);
                 }
             }
             __syncwarp();

@@ -27,6 +27,8 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Suspends until the phase completes or a time limit of the hardware's passes; true if it
+// completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -43,9 +45,29 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// Non-blocking test of the phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase of parity `parity` to complete.  Gives up (returns false) after
-// `limit_ns` nanoseconds so that a lost completion can never hang the GPU.
+// `limit_ns` nanoseconds so that a lost completion can never hang the GPU.  A try_wait may
+// suspend for the hardware's own time limit, so limits below a millisecond are honoured by
+// polling with test_wait instead.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (limit_ns < 1000000ull) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_test_wait(bar, parity))
+            if (global_timer_ns() - t0 > limit_ns) return false;
+        return true;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {

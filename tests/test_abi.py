@@ -73,6 +73,7 @@ def test_plan_worked_example(pda):
     (dict(kv_block_size=64), -2), (dict(head_dim=64), -2), (dict(kv_dtype=3), -2),
     (dict(num_kv_heads=0), -1), (dict(max_blocks_per_seq=0), -1), (dict(tile_groups_per_partition=-1), -1),
     (dict(num_seqs=-1), -1), (dict(max_partitions=-2), -1), (dict(softmax_scale=float("nan")), -1),
+    (dict(wait_timeout_ns=-1), -1),
 ])
 def test_plan_rejects(pda, kw, code):
     args = dict(num_seqs=2, num_kv_heads=2, query_group_size=8, kv_block_size=16, max_blocks_per_seq=4)
