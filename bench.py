@@ -267,10 +267,22 @@ def run_ours(args, rank, world, local_rank):
     inp = wl.generate(w)
     p = pda.plan(w.num_seqs, w.num_kv_heads, w.query_group_size, w.kv_block_size, w.max_blocks_per_seq,
                  w.tile_groups_per_partition, w.max_partitions, w.kv_dtype, w.softmax_scale)
-    q = torch.from_numpy(inp.query.view(np.int16)).to(dev).view(torch.bfloat16)
+    # the step's per-call inputs (query, block table, context lengths) live in one device buffer,
+    # so that the end-to-end loop moves them from host memory with a single copy
+    parts = [inp.query.view(np.uint8).reshape(-1), inp.block_table.view(np.uint8).reshape(-1),
+             inp.context_lens.view(np.uint8).reshape(-1)]
+    offs, total = [], 0
+    for x in parts:
+        offs.append(total)
+        total += (x.size + 255) // 256 * 256
+    step_in_host = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    for x, o in zip(parts, offs):
+        step_in_host[o:o + x.size] = torch.from_numpy(x)
+    step_in = step_in_host.to(dev)
+    q = step_in[offs[0]:offs[0] + parts[0].size].view(torch.bfloat16).view(inp.query.shape)
+    bt = step_in[offs[1]:offs[1] + parts[1].size].view(torch.int32).view(inp.block_table.shape)
+    ctx = step_in[offs[2]:offs[2] + parts[2].size].view(torch.int32)
     cache = torch.from_numpy(inp.cache).to(dev)
-    bt = torch.from_numpy(inp.block_table).to(dev)
-    ctx = torch.from_numpy(inp.context_lens).to(dev)
     ws = pda.workspace(p, dev)
     out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -291,14 +303,17 @@ def run_ours(args, rank, world, local_rank):
     cnt = pda.counters(p, dev)
     launches_per_step = 1 if args.path == "fused" else 2
 
-    def step():
+    def step_on(qx, btx, ctxx, outx):
         if args.path == "fused":
-            pda.decode_fused(p, q, cache, w.num_cache_blocks, bt, ctx, ws["partial_out"], ws["exp_sums"],
-                             ws["max_logits"], cnt, out, err_word=err, stream=stream)
+            pda.decode_fused(p, qx, cache, w.num_cache_blocks, btx, ctxx, ws["partial_out"], ws["exp_sums"],
+                             ws["max_logits"], cnt, outx, err_word=err, stream=stream)
         else:
-            pda.decode(p, q, cache, w.num_cache_blocks, bt, ctx, ws["partial_out"], ws["exp_sums"], ws["max_logits"],
-                       err_word=err, stream=stream)
-            pda.reduce(p, ctx, ws["partial_out"], ws["exp_sums"], ws["max_logits"], out, err_word=err, stream=stream)
+            pda.decode(p, qx, cache, w.num_cache_blocks, btx, ctxx, ws["partial_out"], ws["exp_sums"],
+                       ws["max_logits"], err_word=err, stream=stream)
+            pda.reduce(p, ctxx, ws["partial_out"], ws["exp_sums"], ws["max_logits"], outx, err_word=err, stream=stream)
+
+    def step():
+        step_on(q, bt, ctx, out)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -355,10 +370,11 @@ def run_ours(args, rank, world, local_rank):
     if dist:
         mean_step, mean_dec = max_over_ranks(dist, [mean_step, mean_dec], dev)
 
-    # ---- end to end through the public API with host buffers
-    qh = torch.from_numpy(inp.query.view(np.int16)).view(torch.bfloat16).pin_memory()
-    bth = torch.from_numpy(inp.block_table).pin_memory()
-    ctxh = torch.from_numpy(inp.context_lens).pin_memory()
+    # ---- end to end through the public API with host buffers.  Reported: the C ABI called with the
+    # step's inputs (query, block table, context lengths) and its bf16 output in pinned host
+    # memory, which the kernels read and write across the host link.  Beside it: the same step
+    # with one explicit copy of the packed inputs in and one of the output out.  The KV cache is
+    # device-resident state in both.
     outh = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
     e2e_steps = max(10, min(args.steps, 500))
     e2e = []
@@ -366,9 +382,7 @@ def run_ours(args, rank, world, local_rank):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        q.copy_(qh, non_blocking=True)
-        bt.copy_(bth, non_blocking=True)
-        ctx.copy_(ctxh, non_blocking=True)
+        step_in.copy_(step_in_host, non_blocking=True)
         step()
         outh.copy_(out, non_blocking=True)
         b.record(stream)
@@ -376,8 +390,22 @@ def run_ours(args, rank, world, local_rank):
         if i >= 3:
             e2e.append(a.elapsed_time(b) * 1e-3)
     mean_e2e = sum(e2e) / len(e2e)
+    qh = step_in_host[offs[0]:offs[0] + parts[0].size].view(torch.bfloat16).view(inp.query.shape)
+    bth = step_in_host[offs[1]:offs[1] + parts[1].size].view(torch.int32).view(inp.block_table.shape)
+    ctxh = step_in_host[offs[2]:offs[2] + parts[2].size].view(torch.int32)
+    e2e_zc = []
+    for i in range(e2e_steps + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step_on(qh, bth, ctxh, outh)
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            e2e_zc.append(a.elapsed_time(b) * 1e-3)
+    mean_e2e_zc = sum(e2e_zc) / len(e2e_zc)
     if dist:
-        mean_e2e, = max_over_ranks(dist, [mean_e2e], dev)
+        mean_e2e, mean_e2e_zc = max_over_ranks(dist, [mean_e2e, mean_e2e_zc], dev)
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())}")
@@ -410,9 +438,14 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": committed_traffic(w.name), "kernel": "pda_partition_kernel",
                      "algorithmic_bytes_per_launch": ab["decode"],
                      "peak_source": "measured" if peaks else "fallback"},
-        "e2e": {"value": replica_throughput(world, B_units, mean_e2e), "unit": UNIT,
+        "e2e": {"value": replica_throughput(world, B_units, mean_e2e_zc), "unit": UNIT,
                 "h2d_bytes_per_step": int(qh.numel() * 2 + bth.numel() * 4 + ctxh.numel() * 4),
-                "d2h_bytes_per_step": int(outh.numel() * 2)},
+                "d2h_bytes_per_step": int(outh.numel() * 2),
+                "how": "inputs and output in pinned host memory, read and written by the kernels"},
+        "e2e_with_copies": {"value": replica_throughput(world, B_units, mean_e2e), "unit": UNIT,
+                            "h2d_bytes_per_step": int(step_in_host.numel()),
+                            "d2h_bytes_per_step": int(outh.numel() * 2),
+                            "how": "one copy of the packed inputs in, one copy of the output out"},
         "gpu_launches": launches_per_step * args.steps,
         "step_path": ("pda_decode_fused (one launch)" if args.path == "fused" else "pda_decode + pda_reduce") +
                      (", replayed from a CUDA graph" if args.graph else ""),

@@ -115,6 +115,9 @@ PDA_API int pda_plan(pda_plan_t* plan);
 /*
  * pda_decode -- the partition pass (tq_decode_kernel: steps B to G).
  *   query          device, bf16 [B][Hk*QG][D] contiguous, 16-byte aligned.
+ *                  query, block_table and context_lens may instead be pinned host memory that
+ *                  the device can address (cudaHostAlloc, or cudaHostRegister, under unified
+ *                  addressing): the kernels then read them across the host link, with no copy.
  *   kv_cache       device, bytes [num_cache_blocks][cache_block_bytes], 16-byte aligned.
  *   num_cache_blocks  NB >= 1, < 2^31; block ids outside [0, NB) are data errors.
  *   block_table    device, int32 [B][max_blocks_per_seq]; only entries t/BS for t < ctx are read.
@@ -140,6 +143,7 @@ PDA_API int pda_decode(const pda_plan_t* plan, const void* query, const void* kv
  *   M = max_p m_p,  w_p = l_p * exp(m_p - M),  out = sum_p (w_p / sum_q w_q) * o_p
  * over p < ceil(ctx_b / W).  One partition is copied bit for bit; ctx 0 gives 0.
  *   out            device, [B][Hk*QG][D], bf16 (PDA_OUT_BF16, round to nearest even) or fp32.
+ *                  out and context_lens may be pinned host memory, as for pda_decode's inputs.
  * A context length out of range gives 0 and sets PDA_ERRW_BAD_CONTEXT_LEN.
  */
 PDA_API int pda_reduce(const pda_plan_t* plan, const int* context_lens, const float* partial_out,
@@ -179,6 +183,7 @@ PDA_API int pda_append_kv(const pda_plan_t* plan, const void* k_new, const void*
  *              leaves them zero.  After a call that set PDA_ERRW_PIPELINE_TIMEOUT, zero them
  *              again before the next call.
  *   out, out_dtype                      as for pda_reduce
+ * query, block_table, context_lens and out may be pinned host memory, as for pda_decode.
  * Calls that share counters or partials race if they overlap on the GPU.
  */
 PDA_API int pda_decode_fused(const pda_plan_t* plan, const void* query, const void* kv_cache,

@@ -127,9 +127,12 @@ def workspace(p: Plan, device, fill: float | None = None) -> dict:
     return {"partial_out": mk(so), "exp_sums": mk(ss), "max_logits": mk(ss)}
 
 
-def _need(t: torch.Tensor, name: str, dtype, numel: int):
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+def _need(t: torch.Tensor, name: str, dtype, numel: int, host_ok: bool = False):
+    """Pointer of a contiguous tensor of at least `numel` bytes.  With host_ok, pinned host memory
+    is accepted too: the kernels then read or write it across the host link (unified addressing
+    gives pinned memory one address on both sides)."""
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or (host_ok and t.device.type == "cpu" and t.is_pinned())):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or pinned host memory" if host_ok else ""))
     if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
         raise ValueError(f"{name} has dtype {t.dtype}")
     if not t.is_contiguous():
@@ -149,11 +152,11 @@ def decode(p: Plan, query, kv_cache, num_cache_blocks: int, block_table, context
     """pda_decode: the partition pass (see include/pda.h)."""
     B, Hk, QG, D, P = p.num_seqs, p.num_kv_heads, p.query_group_size, p.head_dim, p.num_partitions
     args = (
-        _need(query, "query", (torch.bfloat16, torch.int16, torch.uint16), B * Hk * QG * D * 2),
+        _need(query, "query", (torch.bfloat16, torch.int16, torch.uint16), B * Hk * QG * D * 2, host_ok=True),
         _need(kv_cache, "kv_cache", None, num_cache_blocks * p.cache_block_bytes),
         ctypes.c_longlong(num_cache_blocks),
-        _need(block_table, "block_table", torch.int32, B * p.max_blocks_per_seq * 4),
-        _need(context_lens, "context_lens", torch.int32, B * 4),
+        _need(block_table, "block_table", torch.int32, B * p.max_blocks_per_seq * 4, host_ok=True),
+        _need(context_lens, "context_lens", torch.int32, B * 4, host_ok=True),
         _need(partial_out, "partial_out", torch.float32, B * Hk * P * QG * D * 4),
         _need(exp_sums, "exp_sums", torch.float32, B * Hk * P * QG * 4),
         _need(max_logits, "max_logits", torch.float32, B * Hk * P * QG * 4),
@@ -170,11 +173,11 @@ def reduce(p: Plan, context_lens, partial_out, exp_sums, max_logits, out, err_wo
     B, Hk, QG, D, P = p.num_seqs, p.num_kv_heads, p.query_group_size, p.head_dim, p.num_partitions
     out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     args = (
-        _need(context_lens, "context_lens", torch.int32, B * 4),
+        _need(context_lens, "context_lens", torch.int32, B * 4, host_ok=True),
         _need(partial_out, "partial_out", torch.float32, B * Hk * P * QG * D * 4),
         _need(exp_sums, "exp_sums", torch.float32, B * Hk * P * QG * 4),
         _need(max_logits, "max_logits", torch.float32, B * Hk * P * QG * 4),
-        _need(out, "out", (torch.float32, torch.bfloat16), B * Hk * QG * D * out.element_size()),
+        _need(out, "out", (torch.float32, torch.bfloat16), B * Hk * QG * D * out.element_size(), host_ok=True),
         ctypes.c_int(out_dtype),
         None if err_word is None else _need(err_word, "err_word", torch.int32, 4),
         _stream(stream),
@@ -215,16 +218,16 @@ def decode_fused(p: Plan, query, kv_cache, num_cache_blocks: int, block_table, c
     B, Hk, QG, D, P = p.num_seqs, p.num_kv_heads, p.query_group_size, p.head_dim, p.num_partitions
     out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     args = (
-        _need(query, "query", (torch.bfloat16, torch.int16, torch.uint16), B * Hk * QG * D * 2),
+        _need(query, "query", (torch.bfloat16, torch.int16, torch.uint16), B * Hk * QG * D * 2, host_ok=True),
         _need(kv_cache, "kv_cache", None, num_cache_blocks * p.cache_block_bytes),
         ctypes.c_longlong(num_cache_blocks),
-        _need(block_table, "block_table", torch.int32, B * p.max_blocks_per_seq * 4),
-        _need(context_lens, "context_lens", torch.int32, B * 4),
+        _need(block_table, "block_table", torch.int32, B * p.max_blocks_per_seq * 4, host_ok=True),
+        _need(context_lens, "context_lens", torch.int32, B * 4, host_ok=True),
         _need(partial_out, "partial_out", torch.float32, B * Hk * P * QG * D * 4),
         _need(exp_sums, "exp_sums", torch.float32, B * Hk * P * QG * 4),
         _need(max_logits, "max_logits", torch.float32, B * Hk * P * QG * 4),
         _need(counters, "counters", torch.int32, B * Hk * 4),
-        _need(out, "out", (torch.float32, torch.bfloat16), B * Hk * QG * D * out.element_size()),
+        _need(out, "out", (torch.float32, torch.bfloat16), B * Hk * QG * D * out.element_size(), host_ok=True),
         ctypes.c_int(out_dtype),
         None if err_word is None else _need(err_word, "err_word", torch.int32, 4),
         _stream(stream),

@@ -1,5 +1,5 @@
 """GPU robustness checks through the C ABI: the bounded-wait error path, cache blocks past 4 GiB,
-and guard words around every buffer the kernels write.
+guard words around every buffer the kernels write, and inputs and output in pinned host memory.
 
 The timeout test makes the kernel's own waits run out (a 1 ns limit is shorter than any tile's
 copy latency); nothing faults or hangs: a warp that gives up still waits, with the default 1 s
@@ -115,3 +115,25 @@ def test_guard_words_around_every_written_buffer_stay_intact(pda, kv):
     assert int(err_buf[0].item()) == SENTINEL_BITS and int(err_buf[2].item()) == SENTINEL_BITS
     # inputs are read only
     assert torch.equal(d["cache"], torch.from_numpy(inp.cache).to("cuda"))
+
+
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
+def test_inputs_and_output_in_pinned_host_memory(pda, kv):
+    # query, block table and context lengths read by the kernels across the host link, the output
+    # written back the same way: the same bits as with every buffer on the device
+    w = wl.small(num_seqs=4, num_kv_heads=2, ctx=(700, 1, 300, 2000), kv_dtype=kv, seed=64)
+    inp = wl.generate(w)
+    d = to_device(inp)
+    p = plan_for(w)
+    ref = _step(pda, p, d, w.num_cache_blocks).cpu()
+    h = {"query": d["query"].cpu().pin_memory(), "block_table": d["block_table"].cpu().pin_memory(),
+         "context_lens": d["context_lens"].cpu().pin_memory(), "cache": d["cache"]}
+    ws = pda.workspace(p, "cuda")
+    out = torch.empty(ref.shape, dtype=torch.float32).pin_memory()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pda.decode(p, h["query"], h["cache"], w.num_cache_blocks, h["block_table"], h["context_lens"], ws["partial_out"],
+               ws["exp_sums"], ws["max_logits"], err_word=err)
+    pda.reduce(p, h["context_lens"], ws["partial_out"], ws["exp_sums"], ws["max_logits"], out, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(out, ref)
