@@ -18,6 +18,7 @@ Contents
                            passages it follows), optionally with per-partition partials.
   * ``e4m3_to_float64()``  the OCP FP8 E4M3 decode written from the format definition.
   * ``e4m3_encode()``      its encode: nearest finite code by brute force, ties to even, saturating.
+  * ``f16_to_float64()``   the IEEE binary16 decode (the TQ4 format's metadata fields).
   * ``append_kv()``        the write side: one new token per sequence into the paged cache.
 
 Parity of every function here is pinned by ``tests/test_oracle_pins.py`` against closed forms,
@@ -43,6 +44,8 @@ _lib = None
 
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
+KV_TQ4 = 2          # the page's 4-bit format: K codes into 16 centroids times k_norm, V codes affine
+TQ4_FIELDS = 3      # fp16 metadata fields per (kv_head, slot): k_norm, v_scale, v_zero
 TOKENS_PER_TILE_GROUP = 256   # KV_COMPUTE_BLOCK: 16 tiles of 16 tokens
 
 
@@ -60,7 +63,8 @@ class _Problem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "num_seqs", "num_kv_heads", "query_group_size", "head_dim", "kv_block_size",
         "max_blocks_per_seq", "kv_dtype", "partition_tokens", "num_partitions",
-        "num_cache_blocks", "cache_block_bytes", "meta_offset_bytes")] + [("softmax_scale", ctypes.c_double)]
+        "num_cache_blocks", "cache_block_bytes", "meta_offset_bytes")] + [("softmax_scale", ctypes.c_double),
+                                                                         ("centroids", ctypes.c_void_p)]
 
 
 def load_library(path: str):
@@ -71,6 +75,8 @@ def load_library(path: str):
         ctypes.c_int64] + [ctypes.c_void_p] * 4
     lib.oracle_e4m3_to_double.restype = ctypes.c_double
     lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_f16_to_double.restype = ctypes.c_double
+    lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_e4m3_encode.restype = ctypes.c_uint8
     lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
     lib.oracle_append_kv.restype = ctypes.c_int
@@ -111,12 +117,16 @@ def cache_layout(num_kv_heads: int, kv_block_size: int, head_dim: int, kv_dtype:
 
     Data region ``[slot][kv_head][K | V]`` (the page's data stride per slot is
     num_kv_heads * bytes-per-slot-per-head), followed by the metadata region
-    ``[kv_head][field][slot]``; fields are fp32 {K scale, V scale} for fp8 and absent for bf16.
+    ``[kv_head][field][slot]``: fp32 {K scale, V scale} for fp8, fp16 {k_norm, v_scale, v_zero}
+    for TQ4 (head_dim/2 bytes of 4-bit codes each for K and V), absent for bf16.
     """
-    elem = 2 if kv_dtype == KV_BF16 else 1
-    token_head_bytes = 2 * head_dim * elem
+    if kv_dtype == KV_TQ4:
+        token_head_bytes = head_dim                      # 2 * head_dim codes of 4 bits
+        meta = num_kv_heads * TQ4_FIELDS * kv_block_size * 2
+    else:
+        token_head_bytes = 2 * head_dim * (2 if kv_dtype == KV_BF16 else 1)
+        meta = 0 if kv_dtype == KV_BF16 else num_kv_heads * 2 * kv_block_size * 4
     data = kv_block_size * num_kv_heads * token_head_bytes
-    meta = 0 if kv_dtype == KV_BF16 else num_kv_heads * 2 * kv_block_size * 4
     return {"token_head_bytes": token_head_bytes, "data_region_bytes": data,
             "meta_offset_bytes": data, "meta_region_bytes": meta,
             "cache_block_bytes": data + meta}
@@ -146,7 +156,7 @@ def e4m3_to_float64(codes, lib=None) -> np.ndarray:
 
 def decode(problem: Problem, query: np.ndarray, cache: np.ndarray, block_table: np.ndarray,
            context_lens: np.ndarray, units=None, partials: bool = False, threads: int | None = None,
-           lib=None):
+           lib=None, centroids=None):
     """Runs the oracle.
 
     query: uint16 bf16 bits [B][Hk*QG][D]; cache: uint8 [NB * cache_block_bytes];
@@ -155,6 +165,7 @@ def decode(problem: Problem, query: np.ndarray, cache: np.ndarray, block_table: 
     float64 [B][Hq][D] (NaN for rows not computed) and, if ``partials``, ``part_o`` [B][Hk][P][QG][D],
     ``part_m``, ``part_l`` [B][Hk][P][QG] (NaN where the partition is empty or not computed),
     plus ``threads`` (the worker threads actually used).  ``lib`` overrides the library.
+    ``centroids``: the 16 float32 centroids of a TQ4 cache (required for that format only).
     """
     lib = lib or _load()
     pr = problem
@@ -170,8 +181,13 @@ def decode(problem: Problem, query: np.ndarray, cache: np.ndarray, block_table: 
     assert cache.size == pr.num_cache_blocks * lay["cache_block_bytes"]
     assert block_table.size == B * pr.max_blocks_per_seq and context_lens.size == B
 
+    cent = None
+    if pr.kv_dtype == KV_TQ4:
+        cent = np.ascontiguousarray(centroids, dtype=np.float32)
+        assert cent.shape == (16,), "a TQ4 cache needs its 16 centroids"
     cp = _Problem(B, Hk, QG, D, pr.kv_block_size, pr.max_blocks_per_seq, pr.kv_dtype, pl["W"], P,
-                  pr.num_cache_blocks, lay["cache_block_bytes"], lay["meta_offset_bytes"], pr.scale)
+                  pr.num_cache_blocks, lay["cache_block_bytes"], lay["meta_offset_bytes"], pr.scale,
+                  None if cent is None else cent.ctypes.data)
 
     out = np.full((B, Hk * QG, D), np.nan)
     po = pm = plv = None
@@ -207,6 +223,12 @@ def decode(problem: Problem, query: np.ndarray, cache: np.ndarray, block_table: 
     return {"out": out, "part_o": po, "part_m": pm, "part_l": plv, "threads": len(chunks)}
 
 
+def f16_to_float64(bits, lib=None) -> np.ndarray:
+    lib = lib or _load()
+    c = np.asarray(bits, dtype=np.uint16)
+    return np.array([lib.oracle_f16_to_double(int(x)) for x in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
 def e4m3_encode(values, lib=None) -> np.ndarray:
     lib = lib or _load()
     v = np.asarray(values, dtype=np.float32)
@@ -231,5 +253,6 @@ def append_kv(problem: Problem, cache: np.ndarray, k_new: np.ndarray, v_new: np.
     rc = lib.oracle_append_kv(ctypes.byref(cp), kn.ctypes.data, vn.ctypes.data, out.ctypes.data, bt.ctypes.data,
                               pos.ctypes.data)
     if rc != 0:
-        raise ValueError({-1: "position outside [0, MB*BS)", -2: "block id outside the pool"}.get(rc, f"oracle error {rc}"))
+        raise ValueError({-1: "position outside [0, MB*BS)", -2: "block id outside the pool",
+                          -4: "no encoder for this cache format"}.get(rc, f"oracle error {rc}"))
     return out

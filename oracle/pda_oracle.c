@@ -31,7 +31,18 @@
  *   - partial epilogue (normalised partial, running max, running sum; sum<=0 treated as 1):
  *     STEP G;   default softmax_scale = 1/sqrt(head_size): module builder.
  * The KV element formats are bf16, or OCP FP8 E4M3 ("e4m3fn") with one fp32 scale per
- * token per KV head for K and for V, kept in the metadata region as [kv_head][K,V][slot].
+ * token per KV head for K and for V, kept in the metadata region as [kv_head][K,V][slot], or
+ * the page's own 4-bit format ("TQ4"), decoded as its STEP F does it:
+ *   - a token-head row is 64 bytes of K codes then 64 bytes of V codes; dimension d is the
+ *     low nibble of byte d/2 when d is even, the high nibble when d is odd (the page reads
+ *     32-bit words and takes nibble n of word w, low bits first, as dimension 8w + n);
+ *   - K element = centroid[code] * k_norm, V element = code * v_scale + v_zero, with k_norm,
+ *     v_scale and v_zero fp16 fields of the metadata region [kv_head][field][slot] and the
+ *     16 fp32 centroids a separate input (STEP A loads them);
+ *   - the page rounds each decoded element to bf16 before its MFMAs; the oracle keeps the
+ *     exact products (the rounding is the kernel's business, as for P);
+ *   - Q is taken as given: the page's Q arrives already rotated (STEP B), so the rotation is
+ *     not part of this computation.
  */
 #include <math.h>
 #include <stdint.h>
@@ -46,16 +57,20 @@ typedef struct {
     int64_t head_dim;          /* D                                   */
     int64_t kv_block_size;     /* BS tokens per cache block           */
     int64_t max_blocks_per_seq;/* MB, row length of the block table   */
-    int64_t kv_dtype;          /* 0 = bf16, 1 = fp8 e4m3 + fp32 scale */
+    int64_t kv_dtype;          /* 0 = bf16, 1 = fp8 e4m3 + fp32 scale, 2 = TQ4 */
     int64_t partition_tokens;  /* W = G * 256                         */
     int64_t num_partitions;    /* P                                   */
     int64_t num_cache_blocks;  /* NB, blocks in the pool              */
     int64_t cache_block_bytes; /* bytes per cache block               */
     int64_t meta_offset_bytes; /* start of the metadata region        */
     double softmax_scale;
+    const float* centroids;    /* TQ4 only: the 16 centroids          */
 } oracle_problem;
 
-enum { ORACLE_OK = 0, ORACLE_BAD_CTX = -1, ORACLE_BAD_BLOCK = -2, ORACLE_NOMEM = -3 };
+enum { KV_BF16 = 0, KV_FP8_E4M3 = 1, KV_TQ4 = 2 };
+enum { TQ4_K_NORM = 0, TQ4_V_SCALE = 1, TQ4_V_ZERO = 2, TQ4_FIELDS = 3 };
+
+enum { ORACLE_OK = 0, ORACLE_BAD_CTX = -1, ORACLE_BAD_BLOCK = -2, ORACLE_NOMEM = -3, ORACLE_UNSUPPORTED = -4 };
 
 /* bf16 is the upper half of an IEEE binary32. */
 static double bf16_bits_to_double(uint16_t h) {
@@ -80,6 +95,19 @@ double oracle_e4m3_to_double(uint8_t x) {
     return sign ? -v : v;
 }
 
+/* IEEE binary16: 1 sign bit, 5 exponent bits with bias 15, 10 mantissa bits; exponent field 0
+ * encodes subnormals m/1024 * 2^-14, field 31 encodes infinity (m = 0) or NaN. */
+double oracle_f16_to_double(uint16_t x) {
+    int sign = (x >> 15) & 1;
+    int e = (x >> 10) & 0x1F;
+    int m = x & 0x3FF;
+    double v;
+    if (e == 0x1F) v = m ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)m / 1024.0, -14);
+    else v = ldexp(1.0 + (double)m / 1024.0, e - 15);
+    return sign ? -v : v;
+}
+
 static float load_f32_le(const uint8_t* p) {
     uint32_t u = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
     float f;
@@ -92,13 +120,34 @@ static uint16_t load_u16_le(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] <
 /* Decodes K (which == 0) or V (which == 1) of token slot `slot`, KV head h, cache block blk. */
 static void decode_row(const oracle_problem* pr, const uint8_t* cache, int64_t blk, int64_t slot,
                        int64_t h, int which, double* dst) {
-    const int64_t D = pr->head_dim;
-    const int64_t elem = pr->kv_dtype == 0 ? 2 : 1;
-    const int64_t token_head_bytes = 2 * D * elem;           /* K bytes then V bytes */
+    const int64_t D = pr->head_dim, BS = pr->kv_block_size;
     const uint8_t* block = cache + blk * pr->cache_block_bytes;
+    if (pr->kv_dtype == KV_TQ4) {
+        /* K codes then V codes, D/2 bytes each, per token-head */
+        const int64_t token_head_bytes = D;
+        const uint8_t* row = block + (slot * pr->num_kv_heads + h) * token_head_bytes + (int64_t)which * (D / 2);
+        const uint8_t* meta = block + pr->meta_offset_bytes + h * TQ4_FIELDS * BS * 2;
+        if (which == 0) {
+            const double k_norm = oracle_f16_to_double(load_u16_le(meta + (TQ4_K_NORM * BS + slot) * 2));
+            for (int64_t d = 0; d < D; ++d) {
+                const int code = (row[d / 2] >> ((d % 2) * 4)) & 0xF;
+                dst[d] = (double)pr->centroids[code] * k_norm;
+            }
+        } else {
+            const double v_scale = oracle_f16_to_double(load_u16_le(meta + (TQ4_V_SCALE * BS + slot) * 2));
+            const double v_zero = oracle_f16_to_double(load_u16_le(meta + (TQ4_V_ZERO * BS + slot) * 2));
+            for (int64_t d = 0; d < D; ++d) {
+                const int code = (row[d / 2] >> ((d % 2) * 4)) & 0xF;
+                dst[d] = (double)code * v_scale + v_zero;
+            }
+        }
+        return;
+    }
+    const int64_t elem = pr->kv_dtype == KV_BF16 ? 2 : 1;
+    const int64_t token_head_bytes = 2 * D * elem;           /* K bytes then V bytes */
     const uint8_t* row = block + slot * pr->num_kv_heads * token_head_bytes + h * token_head_bytes +
                          (int64_t)which * D * elem;
-    if (pr->kv_dtype == 0) {
+    if (pr->kv_dtype == KV_BF16) {
         for (int64_t d = 0; d < D; ++d) dst[d] = bf16_bits_to_double(load_u16_le(row + 2 * d));
     } else {
         /* metadata region: [kv_head][field: 0 = K scale, 1 = V scale][slot] fp32 */
@@ -244,12 +293,15 @@ uint8_t oracle_e4m3_encode(float x) {
  * rounded to fp32, and the scale is stored in the metadata region [kv_head][K,V][slot].
  *   k_new, v_new  bf16 bits [B][Hk][D];  positions int32 [B].
  * Returns ORACLE_OK, ORACLE_BAD_CTX for a position >= MB*BS, ORACLE_BAD_BLOCK for a block id
- * outside the pool (nothing is written for that sequence in either case).
+ * outside the pool (nothing is written for that sequence in either case), ORACLE_UNSUPPORTED for
+ * a TQ4 cache (the pages give no encoder for that format: its rotation and codebook are not on
+ * them).
  */
 int oracle_append_kv(const oracle_problem* pr, const uint16_t* k_new, const uint16_t* v_new, uint8_t* cache,
                      const int32_t* block_table, const int32_t* positions) {
     const int64_t Hk = pr->num_kv_heads, D = pr->head_dim, BS = pr->kv_block_size, MB = pr->max_blocks_per_seq;
     int rc = ORACLE_OK;
+    if (pr->kv_dtype == KV_TQ4) return ORACLE_UNSUPPORTED;
     for (int64_t b = 0; b < pr->num_seqs; ++b) {
         const int64_t pos = positions[b];
         if (pos < 0) continue;
@@ -260,7 +312,7 @@ int oracle_append_kv(const oracle_problem* pr, const uint16_t* k_new, const uint
         for (int64_t h = 0; h < Hk; ++h) {
             for (int which = 0; which < 2; ++which) {
                 const uint16_t* src = (which == 0 ? k_new : v_new) + (b * Hk + h) * D;
-                if (pr->kv_dtype == 0) {
+                if (pr->kv_dtype == KV_BF16) {
                     uint8_t* row = block + (slot * Hk + h) * 2 * D * 2 + (int64_t)which * D * 2;
                     for (int64_t d = 0; d < D; ++d) {
                         row[2 * d] = (uint8_t)(src[d] & 0xFF);

@@ -22,16 +22,28 @@ def problem(w: wl.Workload, G: int | None = None) -> oracle.Problem:
 
 def run_oracle(inp: wl.Inputs, partials=False, G=None, units=None, lib=None, threads=None):
     return oracle.decode(problem(inp.workload, G), inp.query, inp.cache, inp.block_table, inp.context_lens,
-                         units=units, partials=partials, lib=lib, threads=threads)
+                         units=units, partials=partials, lib=lib, threads=threads,
+                         centroids=inp.extra.get("centroids"))
 
 
 def build_from_values(w: wl.Workload, q: np.ndarray, K_list, V_list, table: np.ndarray, poison=True) -> wl.Inputs:
     """Inputs from explicit float32 values (for probes); ctx_b = len(K_list[b])."""
     cache = wl.empty_cache(w, poison)
+    cent = wl.tq4_codebook(w.head_dim) if w.kv_dtype == wl.KV_TQ4 else None
     for b in range(w.num_seqs):
-        wl.write_tokens(w, cache, table[b], K_list[b], V_list[b])
+        wl.write_tokens(w, cache, table[b], K_list[b], V_list[b], cent)
     ctx = np.array([k.shape[0] for k in K_list], dtype=np.int32)
-    return wl.Inputs(w, wl.round_bf16(q), cache, table.astype(np.int32), ctx)
+    return wl.Inputs(w, wl.round_bf16(q), cache, table.astype(np.int32), ctx,
+                     {} if cent is None else {"centroids": cent})
+
+
+def tq4_values(codes: np.ndarray, centroids=None, k_norm_bits=None, v_scale_bits=None, v_zero_bits=None):
+    """Float64 values of unpacked TQ4 codes [..][D] (independent of any reader): K with centroids
+    and k_norm, or V with v_scale and v_zero (fp16 bits, one per row)."""
+    f16 = lambda b: np.asarray(b, dtype=np.uint16).view(np.float16).astype(np.float64)[..., None]
+    if centroids is not None:
+        return np.asarray(centroids, dtype=np.float32).astype(np.float64)[codes] * f16(k_norm_bits)
+    return codes.astype(np.float64) * f16(v_scale_bits) + f16(v_zero_bits)
 
 
 def stored_values(w: wl.Workload, K: np.ndarray):
