@@ -82,8 +82,13 @@ def replica_throughput(world: int, units_per_rank: int, seconds_per_step: float)
     return world * units_per_rank / seconds_per_step
 
 
+KV_NAMES = {wl.KV_BF16: "bf16", wl.KV_FP8_E4M3: "fp8_e4m3", wl.KV_TQ4: "tq4"}
+
+
 def kv_bytes_per_token_head(w: wl.Workload) -> int:
-    return 2 * w.head_dim * w.elem_bytes + (8 if w.kv_dtype == wl.KV_FP8_E4M3 else 0)
+    """K and V bytes of one token of one KV head, metadata fields included (fp8: two fp32
+    scales; TQ4: three fp16 fields)."""
+    return w.token_head_bytes + w.meta_region_bytes // (w.num_kv_heads * w.kv_block_size)
 
 
 def algorithmic_bytes(w: wl.Workload, ctx: np.ndarray, W: int) -> dict:
@@ -244,7 +249,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "global_batch": w.num_seqs, "num_kv_heads": w.num_kv_heads,
-                   "query_group_size": w.query_group_size, "kv_dtype": "bf16" if w.kv_dtype == 0 else "fp8_e4m3"},
+                   "query_group_size": w.query_group_size, "kv_dtype": KV_NAMES[w.kv_dtype]},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
@@ -283,6 +288,10 @@ def run_ours(args, rank, world, local_rank):
     bt = step_in[offs[1]:offs[1] + parts[1].size].view(torch.int32).view(inp.block_table.shape)
     ctx = step_in[offs[2]:offs[2] + parts[2].size].view(torch.int32)
     cache = torch.from_numpy(inp.cache).to(dev)
+    tq4 = w.kv_dtype == wl.KV_TQ4
+    cent = torch.from_numpy(inp.extra["centroids"]).to(dev) if tq4 else None
+    if tq4 and args.path == "fused":
+        raise SystemExit("the fused step does not read TQ4 caches; use --path two")
     ws = pda.workspace(p, dev)
     out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -303,13 +312,20 @@ def run_ours(args, rank, world, local_rank):
     cnt = pda.counters(p, dev)
     launches_per_step = 1 if args.path == "fused" else 2
 
+    def decode_on(qx, btx, ctxx):
+        if tq4:
+            pda.decode_tq4(p, qx, cache, w.num_cache_blocks, cent, btx, ctxx, ws["partial_out"], ws["exp_sums"],
+                           ws["max_logits"], err_word=err, stream=stream)
+        else:
+            pda.decode(p, qx, cache, w.num_cache_blocks, btx, ctxx, ws["partial_out"], ws["exp_sums"],
+                       ws["max_logits"], err_word=err, stream=stream)
+
     def step_on(qx, btx, ctxx, outx):
         if args.path == "fused":
             pda.decode_fused(p, qx, cache, w.num_cache_blocks, btx, ctxx, ws["partial_out"], ws["exp_sums"],
                              ws["max_logits"], cnt, outx, err_word=err, stream=stream)
         else:
-            pda.decode(p, qx, cache, w.num_cache_blocks, btx, ctxx, ws["partial_out"], ws["exp_sums"],
-                       ws["max_logits"], err_word=err, stream=stream)
+            decode_on(qx, btx, ctxx)
             pda.reduce(p, ctxx, ws["partial_out"], ws["exp_sums"], ws["max_logits"], outx, err_word=err, stream=stream)
 
     def step():
@@ -361,8 +377,7 @@ def run_ours(args, rank, world, local_rank):
         flush.zero_()
         a, b = evd[i]
         a.record(stream)
-        pda.decode(p, q, cache, w.num_cache_blocks, bt, ctx, ws["partial_out"], ws["exp_sums"], ws["max_logits"],
-                   err_word=err, stream=stream)
+        decode_on(q, bt, ctx)
         b.record(stream)
     torch.cuda.synchronize()
     t_dec = [a.elapsed_time(b) * 1e-3 for a, b in evd]
@@ -423,7 +438,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": replica_throughput(world, B_units, mean_step), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.kv_dtype == wl.KV_BF16 else "fp8_e4m3",
+        "dtype": KV_NAMES[w.kv_dtype],
         "data": "synthetic",
         "config": {"workload": w.name, "global_batch": world * w.num_seqs, "num_kv_heads": w.num_kv_heads,
                    "query_group_size": w.query_group_size, "kv_block_size": w.kv_block_size,

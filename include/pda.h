@@ -12,7 +12,9 @@
  * Source of the method: the vLLM "tq_decode" page (build_tq_decode_module and the kernel body
  * tq_decode_kernel): argument list, grid (sequence, KV head, partition), block-table walk,
  * partition split with tile_groups_per_partition, mask, online softmax and partial epilogue.
- * The KV element formats here are bf16, or fp8 e4m3 with one fp32 scale per token per KV head.
+ * The KV element formats here are bf16, fp8 e4m3 with one fp32 scale per token per KV head, and
+ * the page's own 4-bit format (TQ4: K codes into 16 centroids times a per-token norm, V codes
+ * with a per-token scale and zero point; pda_decode_tq4).
  *
  * Conventions for every call
  *   - Pointers named "device" are device pointers owned by the caller; the library allocates
@@ -50,7 +52,7 @@ typedef enum pda_status {
     PDA_ERR_CUDA = -6                 /* a CUDA runtime query failed (no device, ...) */
 } pda_status;
 
-enum { PDA_KV_BF16 = 0, PDA_KV_FP8_E4M3 = 1 };
+enum { PDA_KV_BF16 = 0, PDA_KV_FP8_E4M3 = 1, PDA_KV_TQ4 = 2 };
 enum { PDA_OUT_BF16 = 0, PDA_OUT_F32 = 1 };
 
 /* Bits of the device error word. */
@@ -77,7 +79,7 @@ typedef struct pda_plan_t {
     int max_blocks_per_seq;        /* MB, row length of the block table, >= 1                     */
     int tile_groups_per_partition; /* G >= 1, or 0 = smallest G with num_partitions <= max_partitions */
     int max_partitions;            /* cap used when G == 0 (0 = no cap, i.e. G = 1)              */
-    int kv_dtype;                  /* PDA_KV_BF16 or PDA_KV_FP8_E4M3                              */
+    int kv_dtype;                  /* PDA_KV_BF16, PDA_KV_FP8_E4M3 or PDA_KV_TQ4                  */
     float softmax_scale;           /* <= 0 selects 1/sqrt(head_dim)                                */
     int wait_timeout_ns;           /* limit of each bounded wait inside pda_decode's kernel, in
                                       nanoseconds; 0 = 1 s.  A wait that gives up sets
@@ -105,9 +107,11 @@ typedef struct pda_plan_t {
  * ranges (PDA_ERR_INVALID_ARG).
  *
  * Cache block layout (the page's stride block; formats of this library):
- *   data region   [BS slots][Hk heads][K: D elements | V: D elements], elements bf16 or e4m3,
- *   meta region   at meta_offset_bytes, fp8 only: fp32 [Hk][2: K scale, V scale][BS].
- *   cache_block_bytes = BS*Hk*2*D*elem (+ Hk*2*BS*4 for fp8).
+ *   data region   [BS slots][Hk heads][K: D elements | V: D elements], elements bf16, e4m3, or
+ *                 TQ4 4-bit codes (two per byte, dimension 2j in the low nibble of byte j),
+ *   meta region   at meta_offset_bytes: fp8: fp32 [Hk][2: K scale, V scale][BS];
+ *                 TQ4: fp16 [Hk][3: k_norm, v_scale, v_zero][BS]; bf16: none.
+ *   cache_block_bytes = BS*Hk*2*D*elem (+ Hk*2*BS*4 for fp8), or BS*Hk*D + Hk*3*BS*2 for TQ4.
  * Returns PDA_OK, PDA_ERR_INVALID_ARG or PDA_ERR_UNSUPPORTED.
  */
 PDA_API int pda_plan(pda_plan_t* plan);
@@ -132,10 +136,28 @@ PDA_API int pda_plan(pda_plan_t* plan);
  * Data errors: a context length out of range is treated as 0 (nothing written for that
  * sequence) and sets PDA_ERRW_BAD_CONTEXT_LEN; a block id out of range is read as zeros
  * (the tensor copy's out-of-bounds fill) and sets PDA_ERRW_BAD_BLOCK_ID.
+ * A TQ4 plan is rejected (PDA_ERR_INVALID_ARG): that format needs pda_decode_tq4.
  */
 PDA_API int pda_decode(const pda_plan_t* plan, const void* query, const void* kv_cache, long long num_cache_blocks,
                const int* block_table, const int* context_lens, float* partial_out, float* exp_sums,
                float* max_logits, int* err_word, void* stream);
+
+/*
+ * pda_decode_tq4 -- the partition pass for a TQ4 cache (plan->kv_dtype == PDA_KV_TQ4): the
+ * page's own format, decoded as its STEP F does (tq_decode_kernel):
+ *   K[t][d] = centroids[code] * k_norm[t],   V[t][d] = code * v_scale[t] + v_zero[t]
+ * with code the 4-bit code of dimension d of token t (K codes: bytes 0..63 of the token-head
+ * row, V codes: bytes 64..127; dimension 2j in the low nibble of byte j) and the fp16 fields
+ * of the metadata region.  The query is taken as given: on the page it arrives already rotated
+ * into the basis the codes were made in (STEP B), so the rotation is the caller's.
+ *   centroids      device, fp32 [16], finite (STEP A's codebook).
+ * Every other argument, the partial layout and the error rules are those of pda_decode;
+ * pda_reduce combines the partials.  A non-TQ4 plan is rejected (PDA_ERR_INVALID_ARG).
+ */
+PDA_API int pda_decode_tq4(const pda_plan_t* plan, const void* query, const void* kv_cache,
+                           long long num_cache_blocks, const float* centroids, const int* block_table,
+                           const int* context_lens, float* partial_out, float* exp_sums, float* max_logits,
+                           int* err_word, void* stream);
 
 /*
  * pda_reduce -- combines the partials of pda_decode (the reduce that follows the partition
@@ -162,7 +184,8 @@ PDA_API int pda_reduce(const pda_plan_t* plan, const int* context_lens, const fl
  * bf16 caches store the values as given.  fp8 caches store, per (token, KV head) and separately
  * for K and V, scale = absmax / 448 in fp32 (1 when the row is all zero) in the metadata region
  * and codes e4m3(x / scale), both divisions correctly rounded in fp32, the conversion rounding to
- * nearest even and saturating at +-448.
+ * nearest even and saturating at +-448.  TQ4 caches are not supported (PDA_ERR_UNSUPPORTED): the
+ * pages give no encoder for that format (its rotation and codebook are not on them).
  * Data errors (nothing is written for that sequence): a position >= MB*BS sets
  * PDA_ERRW_BAD_POSITION, a block id outside [0, NB) sets PDA_ERRW_BAD_BLOCK_ID.
  * Two sequences whose table entries name the same block and slot race.
@@ -185,6 +208,7 @@ PDA_API int pda_append_kv(const pda_plan_t* plan, const void* k_new, const void*
  *   out, out_dtype                      as for pda_reduce
  * query, block_table, context_lens and out may be pinned host memory, as for pda_decode.
  * Calls that share counters or partials race if they overlap on the GPU.
+ * A TQ4 plan is rejected (PDA_ERR_INVALID_ARG): that format is read by pda_decode_tq4 only.
  */
 PDA_API int pda_decode_fused(const pda_plan_t* plan, const void* query, const void* kv_cache,
                              long long num_cache_blocks, const int* block_table, const int* context_lens,
@@ -209,6 +233,7 @@ PDA_API int pda_decode_fused(const pda_plan_t* plan, const void* query, const vo
  * nothing and frees nothing.
  * All calls share the one array and it keeps the last call's contents (nothing in it needs to
  * start at zero); calls that overlap on the GPU, on any streams, race.
+ * A TQ4 plan is rejected (PDA_ERR_INVALID_ARG): that format is read by pda_decode_tq4 only.
  */
 #define PDA_NOALLOC_SCRATCH_BYTES (64ll << 20)
 PDA_API int pda_decode_step_noalloc(const pda_plan_t* plan, const void* query, const void* kv_cache,

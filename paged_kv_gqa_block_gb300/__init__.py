@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libpda.so")
 
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
+KV_TQ4 = 2
 OUT_BF16 = 0
 OUT_F32 = 1
 ERRW_BAD_CONTEXT_LEN = 1
@@ -77,6 +78,8 @@ def lib():
             L.pda_plan.restype = ctypes.c_int
             L.pda_decode.argtypes = [P, _VP, _VP, ctypes.c_longlong, _VP, _VP, _VP, _VP, _VP, _VP, _VP]
             L.pda_decode.restype = ctypes.c_int
+            L.pda_decode_tq4.argtypes = [P, _VP, _VP, ctypes.c_longlong, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]
+            L.pda_decode_tq4.restype = ctypes.c_int
             L.pda_reduce.argtypes = [P, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, _VP, _VP]
             L.pda_reduce.restype = ctypes.c_int
             L.pda_status_string.argtypes = [ctypes.c_int]
@@ -168,6 +171,28 @@ def decode(p: Plan, query, kv_cache, num_cache_blocks: int, block_table, context
         raise PdaError(rc, "pda_decode")
 
 
+def decode_tq4(p: Plan, query, kv_cache, num_cache_blocks: int, centroids, block_table, context_lens, partial_out,
+               exp_sums, max_logits, err_word=None, stream=None) -> None:
+    """pda_decode_tq4: the partition pass over a TQ4 cache (see include/pda.h); centroids: fp32 [16]."""
+    B, Hk, QG, D, P = p.num_seqs, p.num_kv_heads, p.query_group_size, p.head_dim, p.num_partitions
+    args = (
+        _need(query, "query", (torch.bfloat16, torch.int16, torch.uint16), B * Hk * QG * D * 2, host_ok=True),
+        _need(kv_cache, "kv_cache", None, num_cache_blocks * p.cache_block_bytes),
+        ctypes.c_longlong(num_cache_blocks),
+        _need(centroids, "centroids", torch.float32, 16 * 4),
+        _need(block_table, "block_table", torch.int32, B * p.max_blocks_per_seq * 4, host_ok=True),
+        _need(context_lens, "context_lens", torch.int32, B * 4, host_ok=True),
+        _need(partial_out, "partial_out", torch.float32, B * Hk * P * QG * D * 4),
+        _need(exp_sums, "exp_sums", torch.float32, B * Hk * P * QG * 4),
+        _need(max_logits, "max_logits", torch.float32, B * Hk * P * QG * 4),
+        None if err_word is None else _need(err_word, "err_word", torch.int32, 4),
+        _stream(stream),
+    )
+    rc = lib().pda_decode_tq4(ctypes.byref(p), *args)
+    if rc != 0:
+        raise PdaError(rc, "pda_decode_tq4")
+
+
 def reduce(p: Plan, context_lens, partial_out, exp_sums, max_logits, out, err_word=None, stream=None) -> None:
     """pda_reduce: combines the partials into out [B][Hk*QG][D] (bf16 or fp32 by out's dtype)."""
     B, Hk, QG, D, P = p.num_seqs, p.num_kv_heads, p.query_group_size, p.head_dim, p.num_partitions
@@ -238,15 +263,20 @@ def decode_fused(p: Plan, query, kv_cache, num_cache_blocks: int, block_table, c
 
 
 def decode_step(p: Plan, query, kv_cache, num_cache_blocks: int, block_table, context_lens, ws: dict | None = None,
-                out=None, out_dtype=torch.bfloat16, err_word=None, stream=None):
-    """pda_decode then pda_reduce on one stream; returns out [B][Hk*QG][D]."""
+                out=None, out_dtype=torch.bfloat16, err_word=None, stream=None, centroids=None):
+    """pda_decode (pda_decode_tq4 for a TQ4 plan, with its centroids) then pda_reduce on one stream;
+    returns out [B][Hk*QG][D]."""
     if ws is None:
         ws = workspace(p, query.device)
     if out is None:
         out = torch.empty((p.num_seqs, p.num_kv_heads * p.query_group_size, p.head_dim), dtype=out_dtype,
                           device=query.device)
-    decode(p, query, kv_cache, num_cache_blocks, block_table, context_lens, ws["partial_out"], ws["exp_sums"],
-           ws["max_logits"], err_word=err_word, stream=stream)
+    if p.kv_dtype == KV_TQ4:
+        decode_tq4(p, query, kv_cache, num_cache_blocks, centroids, block_table, context_lens, ws["partial_out"],
+                   ws["exp_sums"], ws["max_logits"], err_word=err_word, stream=stream)
+    else:
+        decode(p, query, kv_cache, num_cache_blocks, block_table, context_lens, ws["partial_out"], ws["exp_sums"],
+               ws["max_logits"], err_word=err_word, stream=stream)
     reduce(p, context_lens, ws["partial_out"], ws["exp_sums"], ws["max_logits"], out, err_word=err_word,
            stream=stream)
     return out

@@ -180,6 +180,11 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// Bytes of K and V of one token of one KV head: 512 (bf16), 256 (fp8), 128 (TQ4 4-bit codes).
+static long long token_head_bytes(int kv_dtype) {
+    return kv_dtype == PDA_KV_BF16 ? 4ll * kHeadDim : kv_dtype == PDA_KV_FP8_E4M3 ? 2ll * kHeadDim : (long long)kHeadDim;
+}
+
 // K|V bytes of one 16-token tile of one KV head.  Dimensions (innermost first):
 //   {128 bytes of a chunk, BS slots, chunks per token-head, Hk heads, NB blocks}
 // with strides {-, Hk*token_head_bytes, 128, token_head_bytes, cache_block_bytes}.  The box
@@ -187,8 +192,7 @@ static EncodeTiledFn encode_fn() {
 static bool encode_kv_map(CUtensorMap* m, const void* cache, const pda_plan_t* p, long long nb) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const int elem = p->kv_dtype == PDA_KV_BF16 ? 2 : 1;
-    const cuuint64_t thb = 2ull * kHeadDim * elem;
+    const cuuint64_t thb = (cuuint64_t)token_head_bytes(p->kv_dtype);
     const cuuint32_t chunks = (cuuint32_t)(thb / 128);
     cuuint64_t dims[5] = {128, (cuuint64_t)p->kv_block_size, chunks, (cuuint64_t)p->num_kv_heads, (cuuint64_t)nb};
     cuuint64_t strides[4] = {(cuuint64_t)p->num_kv_heads * thb, 128, thb, (cuuint64_t)p->cache_block_bytes};
@@ -199,18 +203,22 @@ static bool encode_kv_map(CUtensorMap* m, const void* cache, const pda_plan_t* p
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp8 scales of one 16-token tile: fp32 {BS slots, 2 fields, Hk heads, NB blocks} starting at the
-// metadata region; box {16, 2, 1, 1} lands as [field][token].
+// Metadata of one 16-token tile: {BS slots, F fields, Hk heads, NB blocks} starting at the metadata
+// region; box {16, F, 1, 1} lands as [field][token].  fp8: F = 2 fp32 fields (K scale, V scale);
+// TQ4: F = 3 fp16 fields (k_norm, v_scale, v_zero).
 static bool encode_scale_map(CUtensorMap* m, const void* cache, const pda_plan_t* p, long long nb) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    const bool tq = p->kv_dtype == PDA_KV_TQ4;
+    const cuuint64_t fields = tq ? 3 : 2, esz = tq ? 2 : 4;
     const char* base = static_cast<const char*>(cache) + p->meta_offset_bytes;
-    cuuint64_t dims[4] = {(cuuint64_t)p->kv_block_size, 2, (cuuint64_t)p->num_kv_heads, (cuuint64_t)nb};
-    cuuint64_t strides[3] = {(cuuint64_t)p->kv_block_size * 4, (cuuint64_t)p->kv_block_size * 8,
+    cuuint64_t dims[4] = {(cuuint64_t)p->kv_block_size, fields, (cuuint64_t)p->num_kv_heads, (cuuint64_t)nb};
+    cuuint64_t strides[3] = {(cuuint64_t)p->kv_block_size * esz, (cuuint64_t)p->kv_block_size * esz * fields,
                              (cuuint64_t)p->cache_block_bytes};
-    cuuint32_t box[4] = {(cuuint32_t)kTileTokens, 2, 1, 1};
+    cuuint32_t box[4] = {(cuuint32_t)kTileTokens, (cuuint32_t)fields, 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<char*>(base), dims, strides, box, estr,
+    return fn(m, tq ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<char*>(base),
+              dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -225,7 +233,8 @@ static int compute_plan(const pda_plan_t* in, pda_plan_t* out) {
         return PDA_ERR_UNSUPPORTED;
     if (in->kv_block_size != 16 && in->kv_block_size != 32) return PDA_ERR_UNSUPPORTED;
     if (in->head_dim != kHeadDim) return PDA_ERR_UNSUPPORTED;
-    if (in->kv_dtype != PDA_KV_BF16 && in->kv_dtype != PDA_KV_FP8_E4M3) return PDA_ERR_UNSUPPORTED;
+    if (in->kv_dtype != PDA_KV_BF16 && in->kv_dtype != PDA_KV_FP8_E4M3 && in->kv_dtype != PDA_KV_TQ4)
+        return PDA_ERR_UNSUPPORTED;
     if (!std::isfinite(in->softmax_scale)) return PDA_ERR_INVALID_ARG;
     const long long max_ctx = (long long)in->max_blocks_per_seq * in->kv_block_size;
     if (max_ctx > (1ll << 30)) return PDA_ERR_INVALID_ARG;   // context lengths are int32
@@ -242,9 +251,10 @@ static int compute_plan(const pda_plan_t* in, pda_plan_t* out) {
     const long long units = (long long)in->num_seqs * in->num_kv_heads * P;
     if ((long long)in->num_seqs * in->num_kv_heads > (1ll << 31) - 1 || units * in->query_group_size > (1ll << 40))
         return PDA_ERR_INVALID_ARG;
-    const int elem = in->kv_dtype == PDA_KV_BF16 ? 2 : 1;
-    const long long data = (long long)in->kv_block_size * in->num_kv_heads * 2 * kHeadDim * elem;
-    const long long meta = in->kv_dtype == PDA_KV_BF16 ? 0 : (long long)in->num_kv_heads * 2 * in->kv_block_size * 4;
+    const long long data = (long long)in->kv_block_size * in->num_kv_heads * token_head_bytes(in->kv_dtype);
+    const long long meta = in->kv_dtype == PDA_KV_BF16     ? 0
+                           : in->kv_dtype == PDA_KV_FP8_E4M3 ? (long long)in->num_kv_heads * 2 * in->kv_block_size * 4
+                                                             : (long long)in->num_kv_heads * 3 * in->kv_block_size * 2;
     out->num_partitions = (int)P;
     out->partition_tokens = (int)W;
     out->resolved_tile_groups = (int)G;
@@ -288,8 +298,11 @@ namespace pda {
 static int decode_launch(const pda_plan_t* plan, const void* query, const void* kv_cache, long long num_cache_blocks,
                          const int* block_table, const int* context_lens, float* partial_out, float* exp_sums,
                          float* max_logits, int* err_word, void* stream, bool fused, int* counters, void* out,
-                         int out_dtype) {
+                         int out_dtype, const float* centroids) {
     if (!plan || !plan_matches(plan)) return PDA_ERR_INVALID_ARG;
+    // a TQ4 cache is read only with its centroids (pda_decode_tq4), and only by the two-launch path
+    const bool tq = plan->kv_dtype == PDA_KV_TQ4;
+    if (tq != (centroids != nullptr) || (tq && fused) || ((uintptr_t)centroids & 3u)) return PDA_ERR_INVALID_ARG;
     if (fused && out_dtype != PDA_OUT_BF16 && out_dtype != PDA_OUT_F32) return PDA_ERR_INVALID_ARG;
     if (plan->num_seqs == 0) return PDA_OK;
     if (!query || !kv_cache || !block_table || !context_lens || !partial_out || !exp_sums || !max_logits)
@@ -307,6 +320,7 @@ static int decode_launch(const pda_plan_t* plan, const void* query, const void* 
     a.query = static_cast<const uint16_t*>(query);
     a.block_table = block_table;
     a.context_lens = context_lens;
+    a.centroids = centroids;
     a.partial_out = partial_out;
     a.exp_sums = exp_sums;
     a.max_logits = max_logits;
@@ -331,6 +345,7 @@ static int decode_launch(const pda_plan_t* plan, const void* query, const void* 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (plan->kv_dtype == PDA_KV_BF16) return launch_decode_bf16(a, kv_map, fused, s);
     if (!encode_scale_map(&sc_map, kv_cache, plan, num_cache_blocks)) return PDA_ERR_LAUNCH;
+    if (tq) return launch_decode_tq4(a, kv_map, sc_map, s);
     return launch_decode_fp8(a, kv_map, sc_map, fused, s);
 }
 }  // namespace pda
@@ -341,14 +356,22 @@ int pda_decode(const pda_plan_t* plan, const void* query, const void* kv_cache, 
                const int* block_table, const int* context_lens, float* partial_out, float* exp_sums,
                float* max_logits, int* err_word, void* stream) {
     return decode_launch(plan, query, kv_cache, num_cache_blocks, block_table, context_lens, partial_out, exp_sums,
-                         max_logits, err_word, stream, false, nullptr, nullptr, PDA_OUT_BF16);
+                         max_logits, err_word, stream, false, nullptr, nullptr, PDA_OUT_BF16, nullptr);
+}
+
+int pda_decode_tq4(const pda_plan_t* plan, const void* query, const void* kv_cache, long long num_cache_blocks,
+                   const float* centroids, const int* block_table, const int* context_lens, float* partial_out,
+                   float* exp_sums, float* max_logits, int* err_word, void* stream) {
+    if (!plan || plan->kv_dtype != PDA_KV_TQ4 || !centroids) return PDA_ERR_INVALID_ARG;
+    return decode_launch(plan, query, kv_cache, num_cache_blocks, block_table, context_lens, partial_out, exp_sums,
+                         max_logits, err_word, stream, false, nullptr, nullptr, PDA_OUT_BF16, centroids);
 }
 
 int pda_decode_fused(const pda_plan_t* plan, const void* query, const void* kv_cache, long long num_cache_blocks,
                      const int* block_table, const int* context_lens, float* partial_out, float* exp_sums,
                      float* max_logits, int* counters, void* out, int out_dtype, int* err_word, void* stream) {
     return decode_launch(plan, query, kv_cache, num_cache_blocks, block_table, context_lens, partial_out, exp_sums,
-                         max_logits, err_word, stream, true, counters, out, out_dtype);
+                         max_logits, err_word, stream, true, counters, out, out_dtype, nullptr);
 }
 
 int pda_reduce(const pda_plan_t* plan, const int* context_lens, const float* partial_out, const float* exp_sums,

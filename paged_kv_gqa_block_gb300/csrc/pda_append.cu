@@ -83,6 +83,7 @@ extern "C" int pda_append_kv(const pda_plan_t* plan, const void* k_new, const vo
                              long long num_cache_blocks, const int* block_table, const int* positions, int* err_word,
                              void* stream) {
     if (!plan || pda_workspace_size(plan) < 0) return PDA_ERR_INVALID_ARG;
+    if (plan->kv_dtype == PDA_KV_TQ4) return PDA_ERR_UNSUPPORTED;   // no encoder for that format
     if (plan->num_seqs == 0) return PDA_OK;
     if (!k_new || !v_new || !kv_cache || !block_table || !positions) return PDA_ERR_INVALID_ARG;
     if (num_cache_blocks < 1 || num_cache_blocks > (1ll << 31) - 1) return PDA_ERR_INVALID_ARG;

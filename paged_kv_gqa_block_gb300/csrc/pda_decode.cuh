@@ -24,6 +24,12 @@
 //     fp8 KV: e4m3 -> f16 conversion (exact), Q scaled by a power of two into f16 range,
 //     K scales applied to the fp32 scores, V scales folded into P relative to the tile's
 //     largest V scale (the factor is carried in the running rescale).
+//     TQ4 KV (the page's own 4-bit format, STEP F): K codes become f16 centroid pairs through a
+//     256-entry table in shared memory (one byte = two dimensions), k_norm scales the fp32
+//     scores; V codes enter the PV MMA as exact f16 integers (the code itself as a subnormal
+//     bit pattern, code * 2^-24), v_scale is folded into P like fp8's V scale, and v_zero
+//     contributes sum_t p_t v_zero_t to every dimension, kept per query row beside the
+//     running sum.
 //   * The epilogue stages the partial through the stage it has just consumed and writes it
 //     with coalesced 16-byte stores.
 //   * Every wait is bounded; a wait that gives up sets PDA_ERRW_PIPELINE_TIMEOUT, and the
@@ -46,15 +52,21 @@ constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-template <bool FP8, int S>
+template <int KV, int S>
 struct DecodeCfg {
+    static constexpr bool kBf16 = KV == PDA_KV_BF16, kTq = KV == PDA_KV_TQ4;
     static constexpr int kThreads = 32;
-    static constexpr int kTileBytes = FP8 ? 4096 : 8192;   // K and V of 16 tokens of one KV head
-    static constexpr int kChunks = FP8 ? 2 : 4;             // 128-byte chunks per token-head
-    static constexpr int kScaleBytes = FP8 ? 128 : 0;       // 16 K scales + 16 V scales
+    // K and V of 16 tokens of one KV head: 8 KB bf16, 4 KB fp8, 2 KB of TQ4 codes
+    static constexpr int kTileBytes = kBf16 ? 8192 : kTq ? 2048 : 4096;
+    static constexpr int kChunks = kTileBytes / 2048;       // 128-byte chunks per token-head
+    // metadata copied per tile: fp8 16 K + 16 V scales (fp32); TQ4 16 x {k_norm, v_scale, v_zero} (fp16)
+    static constexpr int kScaleTx = kBf16 ? 0 : kTq ? 96 : 128;
+    static constexpr int kScaleBytes = kBf16 ? 0 : 128;     // per stage (16-byte aligned slots)
+    static constexpr int kLutBytes = kTq ? 1024 : 0;        // TQ4: f16 centroid pair per code byte
     static constexpr int kOffStages = 0;
     static constexpr int kOffScales = S * kTileBytes;
-    static constexpr int kOffBar = align_up(kOffScales + S * kScaleBytes, 8);
+    static constexpr int kOffLut = align_up(kOffScales + S * kScaleBytes, 16);
+    static constexpr int kOffBar = align_up(kOffLut + kLutBytes, 8);
     static constexpr int kSmemBytes = kOffBar + S * 8 + 1024;   // + base alignment slack
 };
 
@@ -215,9 +227,12 @@ __device__ inline void find_range(const DecodeArgs& a, UnitIt& u, long long& hi)
 }
 
 // ---------------------------------------------------------------------------------------------
-template <bool FP8, int NT, int S, bool FUSED>
+template <int KV, int NT, int S, bool FUSED>
 struct Decode {
-    using Cfg = DecodeCfg<FP8, S>;
+    using Cfg = DecodeCfg<KV, S>;
+    static constexpr bool FP8 = KV == PDA_KV_FP8_E4M3;
+    static constexpr bool TQ = KV == PDA_KV_TQ4;
+    static constexpr bool F16 = KV != PDA_KV_BF16;   // f16 MMAs, Q scaled into f16, V scale folded into P
 
     // ------------------------------------------------------------------ tile feeding
     // The issue side walks (unit, 32-entry chunk) pairs; the entries of the next chunk are
@@ -279,10 +294,10 @@ struct Decode {
         const int phys = __shfl_sync(kFull, f.ent, (f.t >> ts) - f.e0);
         if (lane == 0) {
             const int slot0 = (f.t & ((1 << ts) - 1)) * kTileTokens;
-            mbar_arrive_expect_tx(bar, Cfg::kTileBytes + Cfg::kScaleBytes);
+            mbar_arrive_expect_tx(bar, Cfg::kTileBytes + Cfg::kScaleTx);
             tma_load_5d(sbase + Cfg::kOffStages + stage * Cfg::kTileBytes, kv_map, bar, 0, slot0, 0, f.u.h, phys,
                         f.policy);
-            if constexpr (FP8)
+            if constexpr (F16)
                 tma_load_4d(sbase + Cfg::kOffScales + stage * Cfg::kScaleBytes, sc_map, bar, slot0, 0, f.u.h, phys,
                             f.policy);
             if ((phys < 0 || (long long)phys >= a.num_cache_blocks) && a.err_word)
@@ -309,7 +324,7 @@ struct Decode {
     // ------------------------------------------------------------------ Q of a unit
     // Raw words of the unit's Q rows as this lane needs them (rows >= QG read as zero).
     //   bf16: w[n][2kk + j] = Q[8n + gid][16kk + 8j + 2tig .. +1]  (the mma B fragments)
-    //   fp8:  w[n][c]       = Q[8n + gid][32tig + 2c .. +1]         (converted at unit start)
+    //   fp8, TQ4: w[n][c]   = Q[8n + gid][32tig + 2c .. +1]         (converted at unit start)
     static __device__ __forceinline__ void load_q(const DecodeArgs& a, const UnitIt& u, uint32_t (&w)[NT][16],
                                                   int lane) {
         const int gid = lane >> 2, tig = lane & 3;
@@ -319,7 +334,7 @@ struct Decode {
             if (r < a.QG) {
                 const uint32_t* row = reinterpret_cast<const uint32_t*>(
                     a.query + ((long long)u.b * a.Hk * a.QG + (long long)u.h * a.QG + r) * kHeadDim);
-                if constexpr (FP8) {
+                if constexpr (F16) {
                     const uint4* p4 = reinterpret_cast<const uint4*>(row + tig * 16);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -618,6 +633,156 @@ struct Decode {
         }
     }
 
+    // TQ4 stage layout: per token one 128-byte row, K codes in 16-byte units 0..3 (byte i of the
+    // row holds dimensions 2i and 2i + 1, low nibble first), V codes in units 4..7, swizzled as
+    // above; metadata stage: 16 k_norm, 16 v_scale, 16 v_zero (fp16).  `lut` maps a code byte to
+    // the f16 pair (centroid[low nibble], centroid[high nibble]), both scaled by 2^e (cq holds 2^-e).
+    template <int NTL>
+    static __device__ __forceinline__ void step_tq(const uint32_t (&st)[NTL], const __half* const (&scl)[NTL],
+                                                   const int (&valid)[NTL], float cq, const uint32_t* lut,
+                                                   const uint32_t (&qf)[NT][8][2], float (&acc)[NT][8][4],
+                                                   float (&m2)[NT][2], float (&ls)[NT][2], float (&zs)[NT][2],
+                                                   float& F, int lane) {
+        const int gid = lane >> 2, tig = lane & 3;
+        constexpr int CH = NTL == 1 ? 2 : 1;
+        float s[NTL][NT][4];
+        {
+            // K codes of rows gid and gid+8, bytes 16*tig .. 16*tig+15 (dimensions 32*tig .. 32*tig+31)
+            uint32_t k0[NTL][4], k1[NTL][4];
+            const uint32_t u = (uint32_t)((tig ^ (gid & 7)) << 4);
+#pragma unroll
+            for (int tl = 0; tl < NTL; ++tl) {
+                lds128(st[tl] + gid * 128 + u, k0[tl][0], k0[tl][1], k0[tl][2], k0[tl][3]);
+                lds128(st[tl] + (gid + 8) * 128 + u, k1[tl][0], k1[tl][1], k1[tl][2], k1[tl][3]);
+            }
+            float sx[NTL][CH][NT][4];
+#pragma unroll
+            for (int tl = 0; tl < NTL; ++tl)
+#pragma unroll
+                for (int ch = 0; ch < CH; ++ch)
+#pragma unroll
+                    for (int n = 0; n < NT; ++n)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) sx[tl][ch][n][c] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+                for (int tl = 0; tl < NTL; ++tl) {
+                    // code bytes 2kk (dimensions 32tig + 4kk, +1) and 2kk + 1 (+2, +3) of each row
+                    const int sh = (kk & 1) * 16;
+                    const uint32_t w0 = k0[tl][kk >> 1], w1 = k1[tl][kk >> 1];
+                    const uint32_t a0 = lut[(w0 >> sh) & 0xFFu], a2 = lut[(w0 >> (sh + 8)) & 0xFFu];
+                    const uint32_t a1 = lut[(w1 >> sh) & 0xFFu], a3 = lut[(w1 >> (sh + 8)) & 0xFFu];
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) mma_f16(sx[tl][kk % CH][n], a0, a1, a2, a3, qf[n][kk][0], qf[n][kk][1]);
+                }
+#pragma unroll
+            for (int tl = 0; tl < NTL; ++tl)
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) s[tl][n][c] = CH == 2 ? sx[tl][0][n][c] + sx[tl][CH - 1][n][c] : sx[tl][0][n][c];
+        }
+        // k_norm scales the scores; v_scale is folded into P relative to the step's largest
+        // |v_scale|; v_zero enters the per-row zero-point sum.  Tokens past the context contribute
+        // nothing (their fields may hold anything, NaN included).
+        float w0[NTL], w1[NTL], z0[NTL], z1[NTL];
+        float fv = 0.f;
+#pragma unroll
+        for (int tl = 0; tl < NTL; ++tl) {
+            const bool v0 = gid < valid[tl], v1 = gid + 8 < valid[tl];
+            const float f0 = cq * __half2float(scl[tl][gid]), f1 = cq * __half2float(scl[tl][gid + 8]);
+            w0[tl] = v0 ? __half2float(scl[tl][16 + gid]) : 0.f;
+            w1[tl] = v1 ? __half2float(scl[tl][24 + gid]) : 0.f;
+            z0[tl] = v0 ? __half2float(scl[tl][32 + gid]) : 0.f;
+            z1[tl] = v1 ? __half2float(scl[tl][40 + gid]) : 0.f;
+            fv = fmaxf(fv, fmaxf(fabsf(w0[tl]), fabsf(w1[tl])));
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                s[tl][n][0] = v0 ? s[tl][n][0] * f0 : -INFINITY;
+                s[tl][n][1] = v0 ? s[tl][n][1] * f0 : -INFINITY;
+                s[tl][n][2] = v1 ? s[tl][n][2] * f1 : -INFINITY;
+                s[tl][n][3] = v1 ? s[tl][n][3] * f1 : -INFINITY;
+            }
+        }
+        fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 4));
+        fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 8));
+        fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 16));
+        if (!(fv > 0.f)) fv = 1.f;
+        const float rF = rcp_approx(fv);
+        const float ratio = F * rF;
+        F = fv;
+#pragma unroll
+        for (int tl = 0; tl < NTL; ++tl) {
+            w0[tl] *= rF;
+            w1[tl] *= rF;
+        }
+        uint32_t b[NTL][NT][2];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float mx = fmaxf(s[0][n][j], s[0][n][j + 2]);
+#pragma unroll
+                for (int tl = 1; tl < NTL; ++tl) mx = fmaxf(mx, fmaxf(s[tl][n][j], s[tl][n][j + 2]));
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+                const float mnew = fmaxf(m2[n][j], mx);
+                const float alpha = ex2(m2[n][j] - mnew);
+                m2[n][j] = mnew;
+                float sum = 0.f, zsum = 0.f;
+#pragma unroll
+                for (int tl = 0; tl < NTL; ++tl) {
+                    const float p0 = ex2(s[tl][n][j] - mnew), p1 = ex2(s[tl][n][j + 2] - mnew);
+                    sum += p0 + p1;
+                    zsum = fmaf(p0, z0[tl], fmaf(p1, z1[tl], zsum));
+                    s[tl][n][j] = p0 * w0[tl];
+                    s[tl][n][j + 2] = p1 * w1[tl];
+                }
+                ls[n][j] = ls[n][j] * alpha + sum;
+                zs[n][j] = zs[n][j] * alpha + zsum;
+                const float ar = alpha * ratio;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    acc[n][m][j] *= ar;
+                    acc[n][m][j + 2] *= ar;
+                }
+            }
+#pragma unroll
+            for (int tl = 0; tl < NTL; ++tl) {
+                b[tl][n][0] = movmatrix_trans(pack_f16(s[tl][n][0], s[tl][n][1]));
+                b[tl][n][1] = movmatrix_trans(pack_f16(s[tl][n][2], s[tl][n][3]));
+            }
+        }
+        // V codes of tokens 2tig, 2tig+1, 2tig+8, 2tig+9: bytes 8*gid .. 8*gid+7 of the V codes
+        // (dimensions 16*gid .. 16*gid+15), i.e. 16-byte unit 4 + gid/2 from byte 8*(gid&1).  M row
+        // gid <-> d = 16*gid + 2m (low nibble of byte m), M row gid+8 <-> d + 1 (high nibble).  A code
+        // c enters the MMA as the f16 bit pattern c, the subnormal c * 2^-24 (exact); the epilogue
+        // scales by 2^24.
+        const int vu = 4 + (gid >> 1), vo = (gid & 1) << 3;
+        const int x = 2 * tig, y = 2 * tig + 1, x2 = 2 * tig + 8, y2 = 2 * tig + 9;
+#pragma unroll
+        for (int tl = 0; tl < NTL; ++tl) {
+            uint32_t vx[2], vy[2], vx2[2], vy2[2];
+            lds64(st[tl] + x * 128 + ((vu ^ (x & 7)) << 4) + vo, vx[0], vx[1]);
+            lds64(st[tl] + y * 128 + ((vu ^ (y & 7)) << 4) + vo, vy[0], vy[1]);
+            lds64(st[tl] + x2 * 128 + ((vu ^ (x2 & 7)) << 4) + vo, vx2[0], vx2[1]);
+            lds64(st[tl] + y2 * 128 + ((vu ^ (y2 & 7)) << 4) + vo, vy2[0], vy2[1]);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int j = m >> 2;
+                const uint32_t sel = (uint32_t)(m & 3) * 0x0011u + (uint32_t)(4 + (m & 3)) * 0x1100u;
+                const uint32_t t01 = __byte_perm(vx[j], vy[j], sel);     // bytes {x, x, y, y}
+                const uint32_t t23 = __byte_perm(vx2[j], vy2[j], sel);
+                const uint32_t a0 = t01 & 0x000F000Fu, a1 = (t01 >> 4) & 0x000F000Fu;
+                const uint32_t a2 = t23 & 0x000F000Fu, a3 = (t23 >> 4) & 0x000F000Fu;
+#pragma unroll
+                for (int n = 0; n < NT; ++n) mma_f16(acc[n][m], a0, a1, a2, a3, b[tl][n][0], b[tl][n][1]);
+            }
+        }
+    }
+
     // ------------------------------------------------------------------ fused step: output
     static __device__ __forceinline__ void store_out(const DecodeArgs& a, long long orow, int lane, float4 v) {
         if (a.out_f32) {
@@ -742,7 +907,7 @@ struct Decode {
             for (int s = 0; s < S; ++s) mbar_init(bar0 + 8 * s, 1);
             fence_mbar_init();
             prefetch_tensormap(kv_map);
-            if (FP8) prefetch_tensormap(sc_map);
+            if (F16) prefetch_tensormap(sc_map);
         }
         __syncwarp();
         allow_dependent_launch();   // the reduce may be scheduled as soon as CTAs of this grid retire
@@ -756,6 +921,8 @@ struct Decode {
         // Q rows and the first block-table entries are requested before anything waits
         uint32_t qn[NT][16];
         load_q(a, cu, qn, lane);
+        float cent = 0.f;
+        if constexpr (TQ) cent = __ldg(a.centroids + (lane & 15));
         Feed f;
         feed_init(a, hi, cu, f, lane);
         // fill the ring, then look up the next chunk
@@ -764,6 +931,29 @@ struct Decode {
             if (feed_one(a, hi, kv_map, sc_map, sbase, bar0 + 8 * s, s, f, lane)) ++issued;
         if (f.valid && !f.pf) prefetch_next(a, hi, f, lane);
 
+        // TQ4: the 16 centroids, scaled by a power of two into f16 range (each keeps 11 significant
+        // bits), as a table of f16 pairs indexed by one byte of codes (low nibble -> low half)
+        const uint32_t* lut = reinterpret_cast<const uint32_t*>(smem + Cfg::kOffLut);
+        float cscale = 1.f;
+        if constexpr (TQ) {
+            float amax = fabsf(cent);
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+            int e = 0;
+            if (amax > 0.f) e = 14 - ((int)((__float_as_uint(amax) >> 23) & 0xFF) - 127);
+            e = max(-100, min(100, e));
+            cscale = __uint_as_float((uint32_t)(127 - e) << 23);
+            const uint32_t h = (uint32_t)__half_as_ushort(__float2half_rn(cent * __uint_as_float((uint32_t)(e + 127) << 23)));
+            uint32_t* lut_w = reinterpret_cast<uint32_t*>(smem + Cfg::kOffLut);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int x = 8 * lane + i;   // code byte: low nibble 8*(lane&1) + i, high nibble lane/2
+                const uint32_t lo = __shfl_sync(kFull, h, x & 15), hi16 = __shfl_sync(kFull, h, x >> 4);
+                lut_w[x] = lo | (hi16 << 16);
+            }
+            __syncwarp();
+        }
+
         int cs = 0;                          // next stage to consume and its barrier phase
         uint32_t cph = 0;
         bool ok = true;
@@ -771,7 +961,7 @@ struct Decode {
             // ---- unit start: Q fragments, next unit's Q in flight
             uint32_t qf[NT][8][2];
             float cq = a.qk_scale_log2;
-            if constexpr (!FP8) {
+            if constexpr (!F16) {
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -793,7 +983,7 @@ struct Decode {
                 if (amax > 0.f) e = 14 - ((int)((__float_as_uint(amax) >> 23) & 0xFF) - 127);
                 e = max(-100, min(100, e));
                 const float pw = __uint_as_float((uint32_t)(e + 127) << 23);
-                cq = a.qk_scale_log2 * __uint_as_float((uint32_t)(127 - e) << 23);
+                cq = a.qk_scale_log2 * __uint_as_float((uint32_t)(127 - e) << 23) * cscale;
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -809,7 +999,7 @@ struct Decode {
             if (has_next && (nx.b != cu.b || nx.h != cu.h)) load_q(a, nx, qn, lane);   // else: same rows
 
             float acc[NT][8][4];
-            float m2[NT][2], ls[NT][2];
+            float m2[NT][2], ls[NT][2], zs[NT][2];
             float F = 1.f;
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
@@ -817,6 +1007,7 @@ struct Decode {
                 for (int m = 0; m < 8; ++m) acc[n][m][0] = acc[n][m][1] = acc[n][m][2] = acc[n][m][3] = 0.f;
                 m2[n][0] = m2[n][1] = -INFINITY;
                 ls[n][0] = ls[n][1] = 0.f;
+                zs[n][0] = zs[n][1] = 0.f;
             }
             const int nt = unit_tiles(cu, a.W);
             const int tok_base = cu.p * a.W;
@@ -836,7 +1027,12 @@ struct Decode {
                     const uint32_t st[2] = {sbase + Cfg::kOffStages + s0 * Cfg::kTileBytes,
                                             sbase + Cfg::kOffStages + s1 * Cfg::kTileBytes};
                     const int vv[2] = {v0, v0 - kTileTokens};
-                    if constexpr (FP8) {
+                    if constexpr (TQ) {
+                        const __half* const sc[2] = {
+                            reinterpret_cast<const __half*>(smem + Cfg::kOffScales + s0 * Cfg::kScaleBytes),
+                            reinterpret_cast<const __half*>(smem + Cfg::kOffScales + s1 * Cfg::kScaleBytes)};
+                        step_tq<2>(st, sc, vv, cq, lut, qf, acc, m2, ls, zs, F, lane);
+                    } else if constexpr (FP8) {
                         const float* const sc[2] = {
                             reinterpret_cast<const float*>(smem + Cfg::kOffScales + s0 * Cfg::kScaleBytes),
                             reinterpret_cast<const float*>(smem + Cfg::kOffScales + s1 * Cfg::kScaleBytes)};
@@ -847,7 +1043,11 @@ struct Decode {
                 } else {
                     const uint32_t st[1] = {sbase + Cfg::kOffStages + s0 * Cfg::kTileBytes};
                     const int vv[1] = {v0};
-                    if constexpr (FP8) {
+                    if constexpr (TQ) {
+                        const __half* const sc[1] = {
+                            reinterpret_cast<const __half*>(smem + Cfg::kOffScales + s0 * Cfg::kScaleBytes)};
+                        step_tq<1>(st, sc, vv, cq, lut, qf, acc, m2, ls, zs, F, lane);
+                    } else if constexpr (FP8) {
                         const float* const sc[1] = {
                             reinterpret_cast<const float*>(smem + Cfg::kOffScales + s0 * Cfg::kScaleBytes)};
                         step_fp8<1>(st, sc, vv, cq, qf, acc, m2, ls, F, lane);
@@ -873,7 +1073,9 @@ struct Decode {
             if (!ok) break;
 
             // ---- epilogue: the last stage is free; stage the normalised partial through it
-            float inv[NT][2];
+            // o = acc * F / l (F: the V-scale factor; TQ4 codes carry another 2^24), plus, for TQ4,
+            // the zero-point sum z / l
+            float inv[NT][2], zq[NT][2];
 #pragma unroll
             for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -883,30 +1085,46 @@ struct Decode {
                     l += __shfl_xor_sync(kFull, l, 8);
                     l += __shfl_xor_sync(kFull, l, 16);
                     ls[n][j] = l;
-                    inv[n][j] = (l > 0.f ? 1.f / l : 0.f) * (FP8 ? F : 1.f);
+                    const float il = l > 0.f ? 1.f / l : 0.f;
+                    inv[n][j] = il * (FP8 ? F : TQ ? F * 16777216.f : 1.f);
+                    zq[n][j] = 0.f;
+                    if constexpr (TQ) {
+                        float z = zs[n][j];
+                        z += __shfl_xor_sync(kFull, z, 4);
+                        z += __shfl_xor_sync(kFull, z, 8);
+                        z += __shfl_xor_sync(kFull, z, 16);
+                        zq[n][j] = z * il;
+                    }
                 }
             float* stg = reinterpret_cast<float*>(smem + Cfg::kOffStages + stage * Cfg::kTileBytes);
             const long long row0 = ((long long)(cu.b * a.Hk + cu.h) * a.P + cu.p) * a.QG;
-            constexpr int kPass = (Cfg::kTileBytes >= NT * 8 * kHeadDim * 4) ? NT : 1;   // n-tiles per pass
+            // one stage holds 16 (bf16), 8 (fp8) or 4 (TQ4) rows of the partial: a pass stages that many
+            // rows, at most the unit's 8*NT
+            constexpr int kStageRows = Cfg::kTileBytes / (kHeadDim * 4);
+            constexpr int kPassRows = kStageRows < NT * 8 ? kStageRows : NT * 8;
 #pragma unroll
-            for (int n0 = 0; n0 < NT; n0 += kPass) {
-                // write [q][d] floats, 16-byte chunk c of row q stored at c ^ (q & 6)
+            for (int r0 = 0; r0 < NT * 8; r0 += kPassRows) {
+                // write [row][d] floats of rows r0 .. r0 + kPassRows - 1 (local row ql = q - r0), 16-byte
+                // chunk c of local row ql stored at c ^ (ql & 6)
 #pragma unroll
-                for (int dn = 0; dn < kPass; ++dn) {
-                    const int n = n0 + dn;
+                for (int n = 0; n < NT; ++n) {
+                    if (n * 8 + 8 <= r0 || n * 8 >= r0 + kPassRows) continue;
 #pragma unroll
                     for (int m = 0; m < 8; ++m)
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
-                            const int q = dn * 8 + 2 * tig + (c & 1);
-                            const int d = FP8 ? (16 * gid + 2 * m + (c >> 1)) : (16 * m + gid + 8 * (c >> 1));
-                            stg[q * kHeadDim + ((((d >> 2) ^ (q & 6))) << 2) + (d & 3)] = acc[n][m][c] * inv[n][c & 1];
+                            const int ql = n * 8 + 2 * tig + (c & 1) - r0;
+                            if (ql < 0 || ql >= kPassRows) continue;   // a pass of 4 rows holds half an n-tile
+                            const int d = F16 ? (16 * gid + 2 * m + (c >> 1)) : (16 * m + gid + 8 * (c >> 1));
+                            float v = acc[n][m][c] * inv[n][c & 1];
+                            if constexpr (TQ) v += zq[n][c & 1];
+                            stg[ql * kHeadDim + ((((d >> 2) ^ (ql & 6))) << 2) + (d & 3)] = v;
                         }
                 }
                 __syncwarp();
-                const int rows = min(kPass * 8, a.QG - n0 * 8);
+                const int rows = min(kPassRows, a.QG - r0);
                 if (FUSED && cu.nv == 1) {   // the partial is the output (the reduce would copy it)
-                    const long long orow = (long long)cu.b * a.Hk * a.QG + (long long)cu.h * a.QG + n0 * 8;
+                    const long long orow = (long long)cu.b * a.Hk * a.QG + (long long)cu.h * a.QG + r0;
                     for (int q = 0; q < rows; ++q) {
                         const float4 v = *reinterpret_cast<const float4*>(stg + q * kHeadDim + ((lane ^ (q & 6)) << 2));
                         store_out(a, orow + q, lane, v);
@@ -914,7 +1132,7 @@ struct Decode {
                 } else {
                     for (int q = 0; q < rows; ++q) {
                         const float4 v = *reinterpret_cast<const float4*>(stg + q * kHeadDim + ((lane ^ (q & 6)) << 2));
-                        *reinterpret_cast<float4*>(a.partial_out + (row0 + n0 * 8 + q) * kHeadDim + (lane << 2)) = v;
+                        *reinterpret_cast<float4*>(a.partial_out + (row0 + r0 + q) * kHeadDim + (lane << 2)) = v;
                     }
                 }
                 __syncwarp();
@@ -970,13 +1188,13 @@ struct Decode {
 
 // MINB: CTAs per SM the register allocation must allow (more resident warps hide the latency of
 // each warp's serial chain of loads, MMAs and shuffles).
-template <bool FP8, int NT, int S, int MINB, bool FUSED>
+template <int KV, int NT, int S, int MINB, bool FUSED>
 __global__ void __launch_bounds__(32, MINB) pda_partition_kernel(const __grid_constant__ CUtensorMap kv_map,
                                                           const __grid_constant__ CUtensorMap sc_map,
                                                           const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Decode<FP8, NT, S, FUSED>::run(a, &kv_map, &sc_map, smem);
+    Decode<KV, NT, S, FUSED>::run(a, &kv_map, &sc_map, smem);
 }
 
 }  // namespace pda

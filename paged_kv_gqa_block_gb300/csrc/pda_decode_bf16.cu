@@ -11,14 +11,14 @@ int launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& kv_map, bool fuse
     // per SM.  QG = 16: 4 stages, 6 CTAs per SM.
     const bool short_units = a.W == kTokensPerTileGroup && (long long)a.B * a.Hk * a.P <= 2048;
     if (fused) {
-        if (a.QG <= 8) return launch_partition<false, 1, 3, 8, true>(a, kv_map, kv_map, stream);
-        return launch_partition<false, 2, 4, 1, true>(a, kv_map, kv_map, stream);
+        if (a.QG <= 8) return launch_partition<PDA_KV_BF16, 1, 3, 8, true>(a, kv_map, kv_map, stream);
+        return launch_partition<PDA_KV_BF16, 2, 4, 1, true>(a, kv_map, kv_map, stream);
     }
     if (a.QG <= 8) {
-        if (short_units) return launch_partition<false, 1, 4, 6, false>(a, kv_map, kv_map, stream);
-        return launch_partition<false, 1, 3, 8, false>(a, kv_map, kv_map, stream);
+        if (short_units) return launch_partition<PDA_KV_BF16, 1, 4, 6, false>(a, kv_map, kv_map, stream);
+        return launch_partition<PDA_KV_BF16, 1, 3, 8, false>(a, kv_map, kv_map, stream);
     }
-    return launch_partition<false, 2, 4, 1, false>(a, kv_map, kv_map, stream);
+    return launch_partition<PDA_KV_BF16, 2, 4, 1, false>(a, kv_map, kv_map, stream);
 }
 
 }  // namespace pda

@@ -10,11 +10,11 @@ int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUte
     // one-warp CTAs with a private ring of S = 4 stages of 4 KB (+128 B of scales); 12 CTAs per SM
     // for QG <= 8 (168 registers), 8 for QG = 16 (which needs the full register budget)
     if (fused) {
-        if (a.QG <= 8) return launch_partition<true, 1, 4, 12, true>(a, kv_map, sc_map, stream);
-        return launch_partition<true, 2, 4, 8, true>(a, kv_map, sc_map, stream);
+        if (a.QG <= 8) return launch_partition<PDA_KV_FP8_E4M3, 1, 4, 12, true>(a, kv_map, sc_map, stream);
+        return launch_partition<PDA_KV_FP8_E4M3, 2, 4, 8, true>(a, kv_map, sc_map, stream);
     }
-    if (a.QG <= 8) return launch_partition<true, 1, 4, 12, false>(a, kv_map, sc_map, stream);
-    return launch_partition<true, 2, 4, 8, false>(a, kv_map, sc_map, stream);
+    if (a.QG <= 8) return launch_partition<PDA_KV_FP8_E4M3, 1, 4, 12, false>(a, kv_map, sc_map, stream);
+    return launch_partition<PDA_KV_FP8_E4M3, 2, 4, 8, false>(a, kv_map, sc_map, stream);
 }
 
 }  // namespace pda

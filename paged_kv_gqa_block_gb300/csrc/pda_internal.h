@@ -17,6 +17,7 @@ struct DecodeArgs {
     const uint16_t* query;     // bf16 [B][Hk*QG][D]
     const int* block_table;    // [B][MB]
     const int* context_lens;   // [B]
+    const float* centroids;    // TQ4 only: [16]
     float* partial_out;        // [B][Hk][P][QG][D]
     float* exp_sums;           // [B][Hk][P][QG]
     float* max_logits;         // [B][Hk][P][QG]
@@ -47,6 +48,7 @@ struct ReduceArgs {
 int launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& kv_map, bool fused, cudaStream_t stream);
 int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, bool fused,
                       cudaStream_t stream);
+int launch_decode_tq4(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, cudaStream_t stream);
 int launch_reduce(const ReduceArgs& r, cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).

@@ -9,10 +9,10 @@
 namespace pda {
 
 // Persistent grid of one-warp CTAs: (SMs x resident CTAs per SM), capped by the number of units.
-template <bool FP8, int NT, int S, int MINB, bool FUSED>
+template <int KV, int NT, int S, int MINB, bool FUSED>
 int launch_partition(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, cudaStream_t stream) {
-    using Cfg = DecodeCfg<FP8, S>;
-    auto kernel = pda_partition_kernel<FP8, NT, S, MINB, FUSED>;
+    using Cfg = DecodeCfg<KV, S>;
+    auto kernel = pda_partition_kernel<KV, NT, S, MINB, FUSED>;
     static int occ_cache[64] = {0};
     static std::mutex mu;
     int dev = 0;

@@ -45,6 +45,7 @@ extern "C" int pda_decode_step_noalloc(const pda_plan_t* plan, const void* query
                                        long long num_cache_blocks, const int* block_table, const int* context_lens,
                                        void* out, int out_dtype, int* err_word, void* stream) {
     if (!plan || pda_workspace_size(plan) < 0) return PDA_ERR_INVALID_ARG;
+    if (plan->kv_dtype == PDA_KV_TQ4) return PDA_ERR_INVALID_ARG;   // TQ4 needs its centroids (pda_decode_tq4)
     if (plan->num_seqs == 0) return PDA_OK;
     const long long rows = (long long)plan->num_seqs * plan->num_kv_heads * plan->num_partitions *
                            plan->query_group_size;

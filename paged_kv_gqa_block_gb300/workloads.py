@@ -100,6 +100,9 @@ WORKLOADS = {
                  tile_groups_per_partition=0, max_partitions=32),
         Workload("b64_hk8_qg6_bs16_fp8_lognormal2048", 64, 8, 6, 16, 1024, 64 * 1024,
                  ("lognormal", 2048, 1.0, 16, 16384), seed=1005, kv_dtype=KV_FP8_E4M3),
+        # the same step with the page's own 4-bit TQ4 cache
+        Workload("b64_hk8_qg6_bs16_tq4_lognormal2048", 64, 8, 6, 16, 1024, 64 * 1024,
+                 ("lognormal", 2048, 1.0, 16, 16384), seed=1006, kv_dtype=KV_TQ4),
     ]
 }
 WORKLOAD_ORDER = list(WORKLOADS)

@@ -10,12 +10,26 @@ SENTINEL_BITS = 0x7FBADBAD   # a NaN payload the kernels never produce
 
 
 def to_device(inp: wl.Inputs, dev="cuda"):
-    return {
+    d = {
         "query": torch.from_numpy(inp.query.view(np.int16)).to(dev).view(torch.bfloat16),
         "cache": torch.from_numpy(inp.cache).to(dev),
         "block_table": torch.from_numpy(np.ascontiguousarray(inp.block_table)).to(dev),
         "context_lens": torch.from_numpy(np.ascontiguousarray(inp.context_lens)).to(dev),
     }
+    if "centroids" in inp.extra:
+        d["centroids"] = torch.from_numpy(np.ascontiguousarray(inp.extra["centroids"], dtype=np.float32)).to(dev)
+    return d
+
+
+def decode_any(p, w, d, ws, err=None):
+    """The partition pass for any cache format (pda_decode_tq4 for TQ4, pda_decode otherwise)."""
+    import paged_kv_gqa_block_gb300 as pda
+    if w.kv_dtype == wl.KV_TQ4:
+        pda.decode_tq4(p, d["query"], d["cache"], w.num_cache_blocks, d["centroids"], d["block_table"],
+                       d["context_lens"], ws["partial_out"], ws["exp_sums"], ws["max_logits"], err_word=err)
+    else:
+        pda.decode(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"],
+                   ws["partial_out"], ws["exp_sums"], ws["max_logits"], err_word=err)
 
 
 def plan_for(w: wl.Workload, G=None):
@@ -39,8 +53,7 @@ def run_gpu(inp: wl.Inputs, G=None, dev="cuda", d=None):
     d = d or to_device(inp, dev)
     ws = sentinel_ws(p, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    pda.decode(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"],
-               ws["partial_out"], ws["exp_sums"], ws["max_logits"], err_word=err)
+    decode_any(p, w, d, ws, err)
     out32 = torch.empty((w.num_seqs, w.num_q_heads, 128), dtype=torch.float32, device=dev)
     out16 = torch.empty((w.num_seqs, w.num_q_heads, 128), dtype=torch.bfloat16, device=dev)
     pda.reduce(p, d["context_lens"], ws["partial_out"], ws["exp_sums"], ws["max_logits"], out32, err_word=err)

@@ -70,7 +70,7 @@ def test_plan_worked_example(pda):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(query_group_size=7), -2), (dict(query_group_size=4), -2), (dict(kv_block_size=8), -2),
-    (dict(kv_block_size=64), -2), (dict(head_dim=64), -2), (dict(kv_dtype=3), -2),
+    (dict(kv_block_size=64), -2), (dict(head_dim=64), -2), (dict(kv_dtype=3), -2), (dict(kv_dtype=-1), -2),
     (dict(num_kv_heads=0), -1), (dict(max_blocks_per_seq=0), -1), (dict(tile_groups_per_partition=-1), -1),
     (dict(num_seqs=-1), -1), (dict(max_partitions=-2), -1), (dict(softmax_scale=float("nan")), -1),
     (dict(wait_timeout_ns=-1), -1),
@@ -107,3 +107,30 @@ def test_launch_argument_errors_without_a_gpu(pda):
     assert L.pda_decode(ctypes.byref(empty), *args) == 0
     assert L.pda_reduce(ctypes.byref(empty), good, good, good, good, good, 0, None, None) == 0
     assert L.pda_workspace_size(None) == -1
+
+
+def test_tq4_entry_point_rules_without_a_gpu(pda):
+    """A TQ4 cache is read only through pda_decode_tq4, with its centroids; the other entry points
+    turn a TQ4 plan away before launching anything."""
+    L = pda.lib()
+    tq = pda.plan(2, 2, 8, 16, 4, kv_dtype=pda.KV_TQ4)
+    assert tq.cache_block_bytes == 16 * 2 * 128 + 2 * 3 * 16 * 2 and tq.meta_offset_bytes == 16 * 2 * 128
+    bf = pda.plan(2, 2, 8, 16, 4)
+    good = ctypes.c_void_p(1 << 20)
+    dec = [good, good, ctypes.c_longlong(8), good, good, good, good, good, None, None]
+    assert L.pda_decode(ctypes.byref(tq), *dec) == -1                           # needs the centroids
+    tq4 = [good, good, ctypes.c_longlong(8), good, good, good, good, good, good, None, None]
+    assert L.pda_decode_tq4(ctypes.byref(bf), *tq4) == -1                       # not a TQ4 plan
+    no_cent = list(tq4)
+    no_cent[3] = None
+    assert L.pda_decode_tq4(ctypes.byref(tq), *no_cent) == -1
+    odd = list(tq4)
+    odd[3] = ctypes.c_void_p((1 << 20) + 2)
+    assert L.pda_decode_tq4(ctypes.byref(tq), *odd) == -1                       # centroids not 4-byte aligned
+    fused = [good, good, ctypes.c_longlong(8), good, good, good, good, good, good, good, ctypes.c_int(0), None, None]
+    assert L.pda_decode_fused(ctypes.byref(tq), *fused) == -1
+    assert L.pda_decode_step_noalloc(ctypes.byref(tq), good, good, ctypes.c_longlong(8), good, good, good,
+                                     ctypes.c_int(0), None, None) == -1
+    assert L.pda_append_kv(ctypes.byref(tq), good, good, good, ctypes.c_longlong(8), good, good, None, None) == -2
+    empty = pda.plan(0, 2, 8, 16, 4, kv_dtype=pda.KV_TQ4)
+    assert L.pda_decode_tq4(ctypes.byref(empty), *tq4) == 0

@@ -12,11 +12,11 @@ import torch
 
 from paged_kv_gqa_block_gb300 import workloads as wl
 from tests import oracle_helpers as oh
-from tests.gpu_helpers import SENTINEL_BITS, plan_for, run_gpu, to_device
+from tests.gpu_helpers import SENTINEL_BITS, decode_any, plan_for, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 
-TOL = {wl.KV_BF16: 2e-3, wl.KV_FP8_E4M3: 1e-2}
+TOL = {wl.KV_BF16: 2e-3, wl.KV_FP8_E4M3: 1e-2, wl.KV_TQ4: 1e-2}
 
 
 @pytest.fixture(scope="module")
@@ -31,13 +31,20 @@ def _step(pda, p, d, nb, err=None, out_dtype=torch.float32, ws=None):
     B, Hq = p.num_seqs, p.num_kv_heads * p.query_group_size
     ws = ws or pda.workspace(p, "cuda")
     out = torch.empty((B, Hq, 128), dtype=out_dtype, device="cuda")
-    pda.decode(p, d["query"], d["cache"], nb, d["block_table"], d["context_lens"], ws["partial_out"],
-               ws["exp_sums"], ws["max_logits"], err_word=err)
+    if p.kv_dtype == wl.KV_TQ4:
+        pda.decode_tq4(p, d["query"], d["cache"], nb, d["centroids"], d["block_table"], d["context_lens"],
+                       ws["partial_out"], ws["exp_sums"], ws["max_logits"], err_word=err)
+    else:
+        pda.decode(p, d["query"], d["cache"], nb, d["block_table"], d["context_lens"], ws["partial_out"],
+                   ws["exp_sums"], ws["max_logits"], err_word=err)
     pda.reduce(p, d["context_lens"], ws["partial_out"], ws["exp_sums"], ws["max_logits"], out, err_word=err)
     torch.cuda.synchronize()
     return out
 
 
+# (not TQ4: its warps are bound by their own arithmetic, every 2 KB tile has landed before its
+# wait begins, so even a 1 ns limit is not reached; the timeout path itself does not depend on
+# the cache format)
 @pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
 def test_wait_timeout_sets_the_error_bit_and_the_next_call_is_correct(oracle_mod, pda, kv):
     # a step big enough to load HBM (every copy then takes microseconds), each wait limited to 1 ns
@@ -83,7 +90,7 @@ def test_cache_blocks_past_4_gib(oracle_mod, pda):
     del big
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
 def test_guard_words_around_every_written_buffer_stay_intact(pda, kv):
     w = wl.small(num_seqs=3, num_kv_heads=2, ctx=(900, 17, 256), kv_dtype=kv, seed=63)
     inp = wl.generate(w)
@@ -103,8 +110,7 @@ def test_guard_words_around_every_written_buffer_stay_intact(pda, kv):
     out_buf, out = guarded(out_n)
     err_buf = torch.full((3,), SENTINEL_BITS, dtype=torch.int32, device="cuda")
     err_buf[1] = 0
-    pda.decode(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"], po, es, ml,
-               err_word=err_buf[1:2])
+    decode_any(p, w, d, {"partial_out": po, "exp_sums": es, "max_logits": ml}, err_buf[1:2])
     pda.reduce(p, d["context_lens"], po, es, ml, out.view(w.num_seqs, w.num_q_heads, 128), err_word=err_buf[1:2])
     torch.cuda.synchronize()
     for name, buf, n in (("partial_out", po_buf, po.numel()), ("exp_sums", es_buf, es.numel()),
@@ -117,7 +123,7 @@ def test_guard_words_around_every_written_buffer_stay_intact(pda, kv):
     assert torch.equal(d["cache"], torch.from_numpy(inp.cache).to("cuda"))
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
 def test_inputs_and_output_in_pinned_host_memory(pda, kv):
     # query, block table and context lengths read by the kernels across the host link, the output
     # written back the same way: the same bits as with every buffer on the device
@@ -127,12 +133,11 @@ def test_inputs_and_output_in_pinned_host_memory(pda, kv):
     p = plan_for(w)
     ref = _step(pda, p, d, w.num_cache_blocks).cpu()
     h = {"query": d["query"].cpu().pin_memory(), "block_table": d["block_table"].cpu().pin_memory(),
-         "context_lens": d["context_lens"].cpu().pin_memory(), "cache": d["cache"]}
+         "context_lens": d["context_lens"].cpu().pin_memory(), "cache": d["cache"], "centroids": d.get("centroids")}
     ws = pda.workspace(p, "cuda")
     out = torch.empty(ref.shape, dtype=torch.float32).pin_memory()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    pda.decode(p, h["query"], h["cache"], w.num_cache_blocks, h["block_table"], h["context_lens"], ws["partial_out"],
-               ws["exp_sums"], ws["max_logits"], err_word=err)
+    decode_any(p, w, h, ws, err)
     pda.reduce(p, h["context_lens"], ws["partial_out"], ws["exp_sums"], ws["max_logits"], out, err_word=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
