@@ -62,11 +62,9 @@ struct DecodeCfg {
     // metadata copied per tile: fp8 16 K + 16 V scales (fp32); TQ4 16 x {k_norm, v_scale, v_zero} (fp16)
     static constexpr int kScaleTx = kBf16 ? 0 : kTq ? 96 : 128;
     static constexpr int kScaleBytes = kBf16 ? 0 : 128;     // per stage (16-byte aligned slots)
-    static constexpr int kLutBytes = kTq ? 1024 : 0;        // TQ4: f16 centroid pair per code byte
     static constexpr int kOffStages = 0;
     static constexpr int kOffScales = S * kTileBytes;
-    static constexpr int kOffLut = align_up(kOffScales + S * kScaleBytes, 16);
-    static constexpr int kOffBar = align_up(kOffLut + kLutBytes, 8);
+    static constexpr int kOffBar = align_up(kOffScales + S * kScaleBytes, 8);
     static constexpr int kSmemBytes = kOffBar + S * 8 + 1024;   // + base alignment slack
 };
 
@@ -755,28 +753,29 @@ struct Decode {
                 b[tl][n][1] = movmatrix_trans(pack_f16(s[tl][n][2], s[tl][n][3]));
             }
         }
-        // V codes of tokens 2tig, 2tig+1, 2tig+8, 2tig+9: bytes 8*gid .. 8*gid+7 of the V codes
-        // (dimensions 16*gid .. 16*gid+15), i.e. 16-byte unit 4 + gid/2 from byte 8*(gid&1).  M row
-        // gid <-> d = 16*gid + 2m (low nibble of byte m), M row gid+8 <-> d + 1 (high nibble).  A code
-        // c enters the MMA as the f16 bit pattern c, the subnormal c * 2^-24 (exact); the epilogue
-        // scales by 2^24.
-        const int vu = 4 + (gid >> 1), vo = (gid & 1) << 3;
-        const int x = 2 * tig, y = 2 * tig + 1, x2 = 2 * tig + 8, y2 = 2 * tig + 9;
+        // V codes by ldmatrix.trans: matrix (token half th, V code unit k = 16-byte unit 4 + k of the
+        // row) is 8 tokens x 8 code pairs; lane (gid, tig) receives, for tokens 8th + 2tig and
+        // 8th + 2tig + 1 (low and high half), the code pair at bytes 16k + 2gid, 16k + 2gid + 1, i.e.
+        // dimensions 32k + 4gid + e, e = 0..3 in bits 4e .. 4e+3 of each half.  M rows of chunk m:
+        // gid <-> d = 32(m >> 1) + 4gid + 2(m & 1), gid+8 <-> d + 1.  A code enters the MMA as an
+        // f16 subnormal, exactly: the low nibble of a byte as c * 2^-24, the high nibble, unshifted,
+        // as 16c * 2^-24 (the epilogue scales rows gid by 2^24 and rows gid+8 by 2^20).
+        const int lmat = lane >> 3, vtok = 8 * (lmat & 1) + (lane & 7);
 #pragma unroll
         for (int tl = 0; tl < NTL; ++tl) {
-            uint32_t vx[2], vy[2], vx2[2], vy2[2];
-            lds64(st[tl] + x * 128 + ((vu ^ (x & 7)) << 4) + vo, vx[0], vx[1]);
-            lds64(st[tl] + y * 128 + ((vu ^ (y & 7)) << 4) + vo, vy[0], vy[1]);
-            lds64(st[tl] + x2 * 128 + ((vu ^ (x2 & 7)) << 4) + vo, vx2[0], vx2[1]);
-            lds64(st[tl] + y2 * 128 + ((vu ^ (y2 & 7)) << 4) + vo, vy2[0], vy2[1]);
+            uint32_t z[2][4];   // [kp][th + 2 * (k & 1)] for k = 2kp + (k & 1)
+#pragma unroll
+            for (int kp = 0; kp < 2; ++kp) {
+                const int u = 4 + 2 * kp + (lmat >> 1);
+                ldsm_x4_trans(st[tl] + vtok * 128 + ((u ^ (vtok & 7)) << 4), z[kp][0], z[kp][1], z[kp][2], z[kp][3]);
+            }
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
-                const int j = m >> 2;
-                const uint32_t sel = (uint32_t)(m & 3) * 0x0011u + (uint32_t)(4 + (m & 3)) * 0x1100u;
-                const uint32_t t01 = __byte_perm(vx[j], vy[j], sel);     // bytes {x, x, y, y}
-                const uint32_t t23 = __byte_perm(vx2[j], vy2[j], sel);
-                const uint32_t a0 = t01 & 0x000F000Fu, a1 = (t01 >> 4) & 0x000F000Fu;
-                const uint32_t a2 = t23 & 0x000F000Fu, a3 = (t23 >> 4) & 0x000F000Fu;
+                const int k = m >> 1;
+                const uint32_t x0 = z[k >> 1][2 * (k & 1)], x1 = z[k >> 1][2 * (k & 1) + 1];   // token halves
+                const uint32_t y0 = (m & 1) ? (x0 >> 8) : x0, y1 = (m & 1) ? (x1 >> 8) : x1;
+                const uint32_t a0 = y0 & 0x000F000Fu, a1 = y0 & 0x00F000F0u;
+                const uint32_t a2 = y1 & 0x000F000Fu, a3 = y1 & 0x00F000F0u;
 #pragma unroll
                 for (int n = 0; n < NT; ++n) mma_f16(acc[n][m], a0, a1, a2, a3, b[tl][n][0], b[tl][n][1]);
             }
@@ -899,7 +898,7 @@ struct Decode {
 
     // ------------------------------------------------------------------ the warp
     static __device__ void run(const DecodeArgs& a, const CUtensorMap* kv_map, const CUtensorMap* sc_map,
-                               uint8_t* smem) {
+                               uint8_t* smem, uint32_t* tq_lut) {
         const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
         const uint32_t sbase = smem_addr(smem);
         const uint32_t bar0 = sbase + Cfg::kOffBar;
@@ -933,7 +932,7 @@ struct Decode {
 
         // TQ4: the 16 centroids, scaled by a power of two into f16 range (each keeps 11 significant
         // bits), as a table of f16 pairs indexed by one byte of codes (low nibble -> low half)
-        const uint32_t* lut = reinterpret_cast<const uint32_t*>(smem + Cfg::kOffLut);
+        const uint32_t* lut = tq_lut;
         float cscale = 1.f;
         if constexpr (TQ) {
             float amax = fabsf(cent);
@@ -944,7 +943,7 @@ struct Decode {
             e = max(-100, min(100, e));
             cscale = __uint_as_float((uint32_t)(127 - e) << 23);
             const uint32_t h = (uint32_t)__half_as_ushort(__float2half_rn(cent * __uint_as_float((uint32_t)(e + 127) << 23)));
-            uint32_t* lut_w = reinterpret_cast<uint32_t*>(smem + Cfg::kOffLut);
+            uint32_t* lut_w = tq_lut;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int x = 8 * lane + i;   // code byte: low nibble 8*(lane&1) + i, high nibble lane/2
@@ -1073,8 +1072,8 @@ struct Decode {
             if (!ok) break;
 
             // ---- epilogue: the last stage is free; stage the normalised partial through it
-            // o = acc * F / l (F: the V-scale factor; TQ4 codes carry another 2^24), plus, for TQ4,
-            // the zero-point sum z / l
+            // o = acc * F / l (F: the V-scale factor; TQ4 codes carry another 2^24, or 2^20 for the
+            // high nibbles), plus, for TQ4, the zero-point sum z / l
             float inv[NT][2], zq[NT][2];
 #pragma unroll
             for (int n = 0; n < NT; ++n)
@@ -1115,9 +1114,12 @@ struct Decode {
                         for (int c = 0; c < 4; ++c) {
                             const int ql = n * 8 + 2 * tig + (c & 1) - r0;
                             if (ql < 0 || ql >= kPassRows) continue;   // a pass of 4 rows holds half an n-tile
-                            const int d = F16 ? (16 * gid + 2 * m + (c >> 1)) : (16 * m + gid + 8 * (c >> 1));
+                            const int d = TQ    ? (32 * (m >> 1) + 4 * gid + 2 * (m & 1) + (c >> 1))
+                                          : F16 ? (16 * gid + 2 * m + (c >> 1))
+                                                : (16 * m + gid + 8 * (c >> 1));
                             float v = acc[n][m][c] * inv[n][c & 1];
-                            if constexpr (TQ) v += zq[n][c & 1];
+                            if constexpr (TQ) v = fmaf(acc[n][m][c], (c >> 1) ? inv[n][c & 1] * 0.0625f : inv[n][c & 1],
+                                                       zq[n][c & 1]);
                             stg[ql * kHeadDim + ((((d >> 2) ^ (ql & 6))) << 2) + (d & 3)] = v;
                         }
                 }
@@ -1193,8 +1195,10 @@ __global__ void __launch_bounds__(32, MINB) pda_partition_kernel(const __grid_co
                                                           const __grid_constant__ CUtensorMap sc_map,
                                                           const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
+    // TQ4 centroid table: static, so that its lookups address it with an immediate offset
+    __shared__ uint32_t tq_lut[KV == PDA_KV_TQ4 ? 256 : 1];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Decode<KV, NT, S, FUSED>::run(a, &kv_map, &sc_map, smem);
+    Decode<KV, NT, S, FUSED>::run(a, &kv_map, &sc_map, smem, tq_lut);
 }
 
 }  // namespace pda
