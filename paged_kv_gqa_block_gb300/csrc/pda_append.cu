@@ -11,6 +11,7 @@
 #include <cstdint>
 
 #include "pda.h"
+#include "pda_ptx.cuh"
 
 namespace pda {
 
@@ -26,12 +27,6 @@ struct AppendArgs {
     int B, Hk, MB, BS, fp8;
 };
 
-// Two fp32 values to two e4m3 codes (round to nearest even, saturating); lo goes to the low byte.
-__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
 
 // One warp per (sequence, KV head); lane l handles head dims 4l .. 4l+3.
 __global__ void __launch_bounds__(256) pda_append_kernel(const AppendArgs a) {

@@ -184,6 +184,13 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint
         : "r"(w));
 }
 
+// Two fp32 values to two e4m3 codes (round to nearest even, saturating), `lo` in the low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // Weight of one partition in the reduce, w_p = l_p * 2^((m_p - M) * log2 e), with every rounding
 // pinned (no contraction) so that the reduce kernel and the fused step's in-kernel merge give
 // the same bits.
