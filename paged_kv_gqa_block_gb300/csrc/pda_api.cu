@@ -198,8 +198,11 @@ static bool encode_kv_map(CUtensorMap* m, const void* cache, const pda_plan_t* p
     cuuint64_t strides[4] = {(cuuint64_t)p->num_kv_heads * thb, 128, thb, (cuuint64_t)p->cache_block_bytes};
     cuuint32_t box[5] = {128, (cuuint32_t)kTileTokens, chunks, 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    // L2 fetches are widened to 256 bytes, or to 128 for TQ4 whose token-head rows are 128 bytes
+    // (256 would also bring the next head's row, which another warp may read much later)
+    const CUtensorMapL2promotion promo = thb >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(cache), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
