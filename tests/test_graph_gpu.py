@@ -20,7 +20,7 @@ def pda():
     return pda
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
 def test_captured_step_replays_and_follows_context_lengths(oracle_mod, pda, kv):
     ctx = (700, 33, 256, 1500)
     w = wl.small(num_seqs=4, num_kv_heads=2, ctx=ctx, kv_dtype=kv, seed=80, max_blocks_per_seq=100)
@@ -30,15 +30,16 @@ def test_captured_step_replays_and_follows_context_lengths(oracle_mod, pda, kv):
     ws = pda.workspace(p, "cuda")
     out = torch.empty((w.num_seqs, w.num_q_heads, 128), dtype=torch.float32, device="cuda")
     s = torch.cuda.Stream()
+    cent = d.get("centroids")
     with torch.cuda.stream(s):     # one direct call first: per-device set-up happens outside capture
         pda.decode_step(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"], ws=ws,
-                        out=out)
+                        out=out, centroids=cent)
     torch.cuda.synchronize()
     direct = out.clone()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         pda.decode_step(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"], ws=ws,
-                        out=out)
+                        out=out, centroids=cent)
     out.zero_()
     g.replay()
     torch.cuda.synchronize()
@@ -48,6 +49,6 @@ def test_captured_step_replays_and_follows_context_lengths(oracle_mod, pda, kv):
     d["context_lens"].copy_(torch.from_numpy(new_ctx))
     g.replay()
     torch.cuda.synchronize()
-    ref = oh.run_oracle(wl.Inputs(w, inp.query, inp.cache, inp.block_table, new_ctx))["out"]
+    ref = oh.run_oracle(wl.Inputs(w, inp.query, inp.cache, inp.block_table, new_ctx, inp.extra))["out"]
     tol = 2e-3 if kv == wl.KV_BF16 else 1e-2
     assert np.abs(out.cpu().numpy() - ref).max() <= tol
