@@ -193,7 +193,8 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------ oracle leg
 def oracle_units_per_s(inp: wl.Inputs, budget_s: float, rng_seed: int = 0):
     """The fp64 oracle as it stands, on the host cores, on a random sample of (sequence, KV head)
-    units of the step sized to about budget_s seconds.  Returns (units/s, threads, description)."""
+    units of the step sized to about budget_s seconds (whole passes over the step's units when the
+    step is smaller than that).  Returns (units/s, threads, description)."""
     import oracle
     from tests import oracle_helpers as oh
     oracle.build()
@@ -205,15 +206,22 @@ def oracle_units_per_s(inp: wl.Inputs, budget_s: float, rng_seed: int = 0):
     t0 = time.perf_counter()
     r = oh.run_oracle(inp, units=order[:n], threads=cores)
     dt = time.perf_counter() - t0
-    done, threads = n, r["threads"]
-    if dt < budget_s and n < len(order):
-        more = int(min(len(order) - n, max(1, n * (budget_s - dt) / max(dt, 1e-3))))
+    done, threads, passes = n, r["threads"], 0
+    while dt < budget_s:
+        if done < len(order):            # first pass: the rest of the units, sized to the budget
+            more = int(min(len(order) - done, max(1, done * (budget_s - dt) / max(dt, 1e-3))))
+            chunk = order[done:done + more]
+        else:                            # the whole step again
+            chunk = order
+            passes += 1
         t1 = time.perf_counter()
-        r = oh.run_oracle(inp, units=order[n:n + more], threads=cores)
+        r = oh.run_oracle(inp, units=chunk, threads=cores)
         dt += time.perf_counter() - t1
-        done += more
+        done += len(chunk)
         threads = max(threads, r["threads"])
-    return done / dt, threads, f"{done} of {len(order)} (sequence, KV head) units drawn at random, {dt:.1f} s"
+    what = (f"{done} units: the step's {len(order)} (sequence, KV head) units {passes + 1} times" if passes
+            else f"{done} of {len(order)} (sequence, KV head) units drawn at random")
+    return done / dt, threads, f"{what}, {dt:.1f} s"
 
 
 def run_reference(args, rank, world):
