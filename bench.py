@@ -191,7 +191,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------ oracle leg
-def oracle_units_per_s(inp: wl.Inputs, budget_s: float, rng_seed: int = 0):
+def oracle_units_per_s(inp: wl.Inputs, budget_s: float, rng_seed: int = 0, threads_cap: int | None = None):
     """The fp64 oracle as it stands, on the host cores, on a random sample of (sequence, KV head)
     units of the step sized to about budget_s seconds (whole passes over the step's units when the
     step is smaller than that).  Returns (units/s, threads, description)."""
@@ -201,7 +201,7 @@ def oracle_units_per_s(inp: wl.Inputs, budget_s: float, rng_seed: int = 0):
     w = inp.workload
     rng = np.random.default_rng(rng_seed)
     order = rng.permutation(w.num_seqs * w.num_kv_heads)
-    cores = os.cpu_count() or 1
+    cores = threads_cap or os.cpu_count() or 1
     n = min(len(order), cores)
     t0 = time.perf_counter()
     r = oh.run_oracle(inp, units=order[:n], threads=cores)
@@ -390,6 +390,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     t_dec = [a.elapsed_time(b) * 1e-3 for a, b in evd]
     mean_step, mean_dec = sum(t_step) / len(t_step), sum(t_dec) / len(t_dec)
+    med_step, min_step = float(np.median(t_step)), min(t_step)
     if dist:
         mean_step, mean_dec = max_over_ranks(dist, [mean_step, mean_dec], dev)
 
@@ -445,6 +446,7 @@ def run_ours(args, rank, world, local_rank):
     res = {
         "metric": METRIC, "value": replica_throughput(world, B_units, mean_step), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_step * 1e3, "higher_is_better": True,
+        "step_ms_median": med_step * 1e3, "step_ms_min": min_step * 1e3,
         "scaling": "weak", "vs_baseline": None,
         "dtype": KV_NAMES[w.kv_dtype],
         "data": "synthetic",
@@ -479,6 +481,8 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_cpu_baseline and world >= 1:
         v, threads, sample = oracle_units_per_s(inp, args.cpu_budget_s)
         res["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+        v1, _, sample1 = oracle_units_per_s(inp, args.cpu_budget_s / 3, threads_cap=1)
+        res["cpu_baseline_1thread"] = {"value": v1, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample1}
     print(json.dumps(res))
     if dist:
         dist.destroy_process_group()
