@@ -356,6 +356,167 @@ struct Decode {
         }
     }
 
+    // ------------------------------------------------------------------ online softmax
+    // The eager update (no kLazy): with scaled V (VS) the V weights are first divided by the step's
+    // largest one, F, and the accumulators rebased on it (ratio); then, n-tile by n-tile, each
+    // query row reduces the step's maximum across the lanes, rescales its state to the new
+    // maximum and adds the step.
+    template <int NTL>
+    static __device__ __forceinline__ float eager_v_rebase(float (&w0)[NTL], float (&w1)[NTL], float& F) {
+        float fv = 0.f;
+#pragma unroll
+        for (int tl = 0; tl < NTL; ++tl) fv = fmaxf(fv, fmaxf(fabsf(w0[tl]), fabsf(w1[tl])));
+        fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 4));
+        fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 8));
+        fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 16));
+        if (!(fv > 0.f)) fv = 1.f;
+        const float rF = rcp_approx(fv);   // acc and F move together: only their product matters
+        const float ratio = F * rF;        // acc holds true_acc / F: rebase it on this step's factor
+        F = fv;
+#pragma unroll
+        for (int tl = 0; tl < NTL; ++tl) {
+            w0[tl] *= rF;
+            w1[tl] *= rF;
+        }
+        return ratio;
+    }
+    template <int NTL, bool VS, bool ZS>
+    static __device__ __forceinline__ void eager_rows(int n, float (&s)[NTL][NT][4], const float (&w0)[NTL],
+                                                      const float (&w1)[NTL], const float (&z0)[NTL],
+                                                      const float (&z1)[NTL], float (&acc)[NT][8][4],
+                                                      float (&m2)[NT][2], float (&ls)[NT][2], float (&zs)[NT][2],
+                                                      float ratio) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float mx = fmaxf(s[0][n][j], s[0][n][j + 2]);
+#pragma unroll
+            for (int tl = 1; tl < NTL; ++tl) mx = fmaxf(mx, fmaxf(s[tl][n][j], s[tl][n][j + 2]));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+            const float mnew = fmaxf(m2[n][j], mx);
+            const float alpha = ex2(m2[n][j] - mnew);
+            m2[n][j] = mnew;
+            float sum = 0.f, zsum = 0.f;
+#pragma unroll
+            for (int tl = 0; tl < NTL; ++tl) {
+                const float p0 = ex2(s[tl][n][j] - mnew), p1 = ex2(s[tl][n][j + 2] - mnew);
+                sum += p0 + p1;
+                if constexpr (ZS) zsum = fmaf(p0, z0[tl], fmaf(p1, z1[tl], zsum));
+                s[tl][n][j] = VS ? p0 * w0[tl] : p0;
+                s[tl][n][j + 2] = VS ? p1 * w1[tl] : p1;
+            }
+            ls[n][j] = ls[n][j] * alpha + sum;
+            if constexpr (ZS) zs[n][j] = zs[n][j] * alpha + zsum;
+            const float ar = alpha * ratio;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                acc[n][m][j] *= ar;
+                acc[n][m][j + 2] *= ar;
+            }
+        }
+    }
+
+    // One step's update of the running softmax state, given the step's scores s (log2 units,
+    // -inf where masked).  The reference point m2 of each query row, and with scaled V (VS) the
+    // factor F that the V weights w are divided by, move lazily: only when a score exceeds m2 by
+    // more than kLazyLog2, or a V weight leaves (F/64, 64F].  Most steps then skip the cross-lane
+    // reductions and the rescale of the accumulators; P = 2^(s - m2) stays below 2^kLazyLog2 and
+    // P w / F below 2^14 (f16 range).  mt keeps this lane's true running maximum (reduced once, in
+    // the epilogue).  On return s holds P, times w/F with scaled V; ls (and zs, the zero-point
+    // sum, with ZS) include the step.
+    //
+    // Without kLazy every step rebases, row by row (m2 is then the running maximum and F the
+    // step's largest V weight).  That order is kept where the lazy form measured slower: the fp8
+    // kernel, whose 168-register budget (12 CTAs per SM) it strains, and QG = 16 (two n-tiles).
+    static constexpr float kLazyLog2 = 8.f;
+    static constexpr bool kLazy = NT == 1 && !FP8;
+    template <int NTL, bool VS, bool ZS>
+    static __device__ __forceinline__ void softmax_step(float (&s)[NTL][NT][4], float (&w0)[NTL], float (&w1)[NTL],
+                                                        const float (&z0)[NTL], const float (&z1)[NTL],
+                                                        float (&acc)[NT][8][4], float (&m2)[NT][2],
+                                                        float (&mt)[NT][2], float (&ls)[NT][2], float (&zs)[NT][2],
+                                                        float& F, float& rF) {
+        float mx[NT][2];
+        bool up = false;
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float x = fmaxf(s[0][n][j], s[0][n][j + 2]);
+#pragma unroll
+                for (int tl = 1; tl < NTL; ++tl) x = fmaxf(x, fmaxf(s[tl][n][j], s[tl][n][j + 2]));
+                mx[n][j] = x;
+                mt[n][j] = fmaxf(mt[n][j], x);
+                up |= x > m2[n][j] + kLazyLog2;
+            }
+        float fl = 0.f;
+        if constexpr (VS) {
+#pragma unroll
+            for (int tl = 0; tl < NTL; ++tl) fl = fmaxf(fl, fmaxf(fabsf(w0[tl]), fabsf(w1[tl])));
+            up |= fl > F * 64.f;
+        }
+        bool need = __any_sync(kFull, up);
+        if constexpr (VS) need = need || __all_sync(kFull, fl < F * 0.015625f);
+        if (need) {   // warp-uniform: move the reference points to this step's maxima
+            float ratio = 1.f;
+            if constexpr (VS) {
+                float fv = fl;
+                fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 4));
+                fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 8));
+                fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 16));
+                if (!(fv > 0.f)) fv = 1.f;
+                const float r = rcp_approx(fv);
+                ratio = F * r;   // acc holds true_acc / F: rebase it on the new factor
+                F = fv;
+                rF = r;
+            }
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float x = mx[n][j];
+                    x = fmaxf(x, __shfl_xor_sync(kFull, x, 4));
+                    x = fmaxf(x, __shfl_xor_sync(kFull, x, 8));
+                    x = fmaxf(x, __shfl_xor_sync(kFull, x, 16));
+                    const float mnew = fmaxf(m2[n][j], x);
+                    const float alpha = mnew == -INFINITY ? 1.f : ex2(m2[n][j] - mnew);
+                    m2[n][j] = mnew;
+                    ls[n][j] *= alpha;
+                    if constexpr (ZS) zs[n][j] *= alpha;
+                    const float ar = alpha * ratio;
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        acc[n][m][j] *= ar;
+                        acc[n][m][j + 2] *= ar;
+                    }
+                }
+        }
+        if constexpr (VS) {
+#pragma unroll
+            for (int tl = 0; tl < NTL; ++tl) {
+                w0[tl] *= rF;
+                w1[tl] *= rF;
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float sum = 0.f, zsum = 0.f;
+#pragma unroll
+                for (int tl = 0; tl < NTL; ++tl) {
+                    const float p0 = ex2(s[tl][n][j] - m2[n][j]), p1 = ex2(s[tl][n][j + 2] - m2[n][j]);
+                    sum += p0 + p1;
+                    if constexpr (ZS) zsum = fmaf(p0, z0[tl], fmaf(p1, z1[tl], zsum));
+                    s[tl][n][j] = VS ? p0 * w0[tl] : p0;
+                    s[tl][n][j + 2] = VS ? p1 * w1[tl] : p1;
+                }
+                ls[n][j] += sum;
+                if constexpr (ZS) zs[n][j] += zsum;
+            }
+    }
+
     // ------------------------------------------------------------------ tile math
     // One step processes NTL (1 or 2) consecutive 16-token tiles of a unit with a single online-
     // softmax update; two tiles give the warp two independent score-MMA chains and halve the
@@ -366,7 +527,8 @@ struct Decode {
     template <int NTL>
     static __device__ __forceinline__ void step_bf16(const uint32_t (&st)[NTL], const int (&valid)[NTL], float scale2,
                                                      const uint32_t (&qf)[NT][8][2], float (&acc)[NT][8][4],
-                                                     float (&m2)[NT][2], float (&ls)[NT][2], int lane) {
+                                                     float (&m2)[NT][2], float (&mt)[NT][2], float (&ls)[NT][2],
+                                                     int lane) {
         const int gid = lane >> 2, tig = lane & 3;
         constexpr int CH = NTL == 1 ? 2 : 1;   // independent MMA chains per tile
         float s[NTL][NT][4];
@@ -411,35 +573,15 @@ struct Decode {
                 s[tl][n][3] = v1 ? s[tl][n][3] * scale2 : -INFINITY;
             }
         }
+        float w[NTL], zz[NTL], zsd[NT][2];
+        if constexpr (kLazy) {
+            float Fd = 1.f, rFd = 1.f;
+            softmax_step<NTL, false, false>(s, w, w, zz, zz, acc, m2, mt, ls, zsd, Fd, rFd);
+        }
         uint32_t bh[NTL][NT][2], bl[NTL][NT][2];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float mx = fmaxf(s[0][n][j], s[0][n][j + 2]);
-#pragma unroll
-                for (int tl = 1; tl < NTL; ++tl) mx = fmaxf(mx, fmaxf(s[tl][n][j], s[tl][n][j + 2]));
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-                const float mnew = fmaxf(m2[n][j], mx);
-                const float alpha = ex2(m2[n][j] - mnew);
-                m2[n][j] = mnew;
-                float sum = 0.f;
-#pragma unroll
-                for (int tl = 0; tl < NTL; ++tl) {
-                    const float p0 = ex2(s[tl][n][j] - mnew), p1 = ex2(s[tl][n][j + 2] - mnew);
-                    s[tl][n][j] = p0;
-                    s[tl][n][j + 2] = p1;
-                    sum += p0 + p1;
-                }
-                ls[n][j] = ls[n][j] * alpha + sum;
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    acc[n][m][j] *= alpha;
-                    acc[n][m][j + 2] *= alpha;
-                }
-            }
+            if constexpr (!kLazy) eager_rows<NTL, false, false>(n, s, w, w, zz, zz, acc, m2, ls, zsd, 1.f);
 #pragma unroll
             for (int tl = 0; tl < NTL; ++tl) {
                 const uint32_t h01 = pack_bf16(s[tl][n][0], s[tl][n][1]);
@@ -489,8 +631,8 @@ struct Decode {
     template <int NTL>
     static __device__ __forceinline__ void step_fp8(const uint32_t (&st)[NTL], const float* const (&scl)[NTL],
                                                     const int (&valid)[NTL], float cq, const uint32_t (&qf)[NT][8][2],
-                                                    float (&acc)[NT][8][4], float (&m2)[NT][2], float (&ls)[NT][2],
-                                                    float& F, int lane) {
+                                                    float (&acc)[NT][8][4], float (&m2)[NT][2], float (&mt)[NT][2],
+                                                    float (&ls)[NT][2], float& F, float& rF, int lane) {
         const int gid = lane >> 2, tig = lane & 3;
         constexpr int CH = NTL == 1 ? 2 : 1;
         float s[NTL][NT][4];
@@ -532,16 +674,14 @@ struct Decode {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) s[tl][n][c] = CH == 2 ? sx[tl][0][n][c] + sx[tl][CH - 1][n][c] : sx[tl][0][n][c];
         }
-        // scales; the V scales are folded into P relative to the step's largest |V scale|
+        // scales; the V scales are folded into P relative to the factor F
         float w0[NTL], w1[NTL];
-        float fv = 0.f;
 #pragma unroll
         for (int tl = 0; tl < NTL; ++tl) {
             const bool v0 = gid < valid[tl], v1 = gid + 8 < valid[tl];
             const float f0 = cq * scl[tl][gid], f1 = cq * scl[tl][gid + 8];
             w0[tl] = v0 ? scl[tl][16 + gid] : 0.f;
             w1[tl] = v1 ? scl[tl][24 + gid] : 0.f;
-            fv = fmaxf(fv, fmaxf(fabsf(w0[tl]), fabsf(w1[tl])));
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 s[tl][n][0] = v0 ? s[tl][n][0] * f0 : -INFINITY;
@@ -550,48 +690,15 @@ struct Decode {
                 s[tl][n][3] = v1 ? s[tl][n][3] * f1 : -INFINITY;
             }
         }
-        fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 4));
-        fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 8));
-        fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 16));
-        if (!(fv > 0.f)) fv = 1.f;
-        const float rF = rcp_approx(fv);   // acc and F move together: only their product matters
-        const float ratio = F * rF;   // acc holds true_acc / F; rebase it on this step's factor
-        F = fv;
-#pragma unroll
-        for (int tl = 0; tl < NTL; ++tl) {
-            w0[tl] *= rF;
-            w1[tl] *= rF;
-        }
+        float zz[NTL], zsd[NT][2], ratio = 1.f;
+        if constexpr (kLazy)
+            softmax_step<NTL, true, false>(s, w0, w1, zz, zz, acc, m2, mt, ls, zsd, F, rF);
+        else
+            ratio = eager_v_rebase<NTL>(w0, w1, F);
         uint32_t b[NTL][NT][2];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float mx = fmaxf(s[0][n][j], s[0][n][j + 2]);
-#pragma unroll
-                for (int tl = 1; tl < NTL; ++tl) mx = fmaxf(mx, fmaxf(s[tl][n][j], s[tl][n][j + 2]));
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-                const float mnew = fmaxf(m2[n][j], mx);
-                const float alpha = ex2(m2[n][j] - mnew);
-                m2[n][j] = mnew;
-                float sum = 0.f;
-#pragma unroll
-                for (int tl = 0; tl < NTL; ++tl) {
-                    const float p0 = ex2(s[tl][n][j] - mnew), p1 = ex2(s[tl][n][j + 2] - mnew);
-                    sum += p0 + p1;
-                    s[tl][n][j] = p0 * w0[tl];
-                    s[tl][n][j + 2] = p1 * w1[tl];
-                }
-                ls[n][j] = ls[n][j] * alpha + sum;
-                const float ar = alpha * ratio;
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    acc[n][m][j] *= ar;
-                    acc[n][m][j + 2] *= ar;
-                }
-            }
+            if constexpr (!kLazy) eager_rows<NTL, true, false>(n, s, w0, w1, zz, zz, acc, m2, ls, zsd, ratio);
 #pragma unroll
             for (int tl = 0; tl < NTL; ++tl) {
                 b[tl][n][0] = movmatrix_trans(pack_f16(s[tl][n][0], s[tl][n][1]));
@@ -639,8 +746,8 @@ struct Decode {
     static __device__ __forceinline__ void step_tq(const uint32_t (&st)[NTL], const __half* const (&scl)[NTL],
                                                    const int (&valid)[NTL], float cq, const uint32_t* lut,
                                                    const uint32_t (&qf)[NT][8][2], float (&acc)[NT][8][4],
-                                                   float (&m2)[NT][2], float (&ls)[NT][2], float (&zs)[NT][2],
-                                                   float& F, int lane) {
+                                                   float (&m2)[NT][2], float (&mt)[NT][2], float (&ls)[NT][2],
+                                                   float (&zs)[NT][2], float& F, float& rF, int lane) {
         const int gid = lane >> 2, tig = lane & 3;
         constexpr int CH = NTL == 1 ? 2 : 1;
         float s[NTL][NT][4];
@@ -681,11 +788,10 @@ struct Decode {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) s[tl][n][c] = CH == 2 ? sx[tl][0][n][c] + sx[tl][CH - 1][n][c] : sx[tl][0][n][c];
         }
-        // k_norm scales the scores; v_scale is folded into P relative to the step's largest
-        // |v_scale|; v_zero enters the per-row zero-point sum.  Tokens past the context contribute
-        // nothing (their fields may hold anything, NaN included).
+        // k_norm scales the scores; v_scale is folded into P relative to the factor F; v_zero
+        // enters the per-row zero-point sum.  Tokens past the context contribute nothing (their
+        // fields may hold anything, NaN included).
         float w0[NTL], w1[NTL], z0[NTL], z1[NTL];
-        float fv = 0.f;
 #pragma unroll
         for (int tl = 0; tl < NTL; ++tl) {
             const bool v0 = gid < valid[tl], v1 = gid + 8 < valid[tl];
@@ -694,7 +800,6 @@ struct Decode {
             w1[tl] = v1 ? __half2float(scl[tl][24 + gid]) : 0.f;
             z0[tl] = v0 ? __half2float(scl[tl][32 + gid]) : 0.f;
             z1[tl] = v1 ? __half2float(scl[tl][40 + gid]) : 0.f;
-            fv = fmaxf(fv, fmaxf(fabsf(w0[tl]), fabsf(w1[tl])));
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 s[tl][n][0] = v0 ? s[tl][n][0] * f0 : -INFINITY;
@@ -703,50 +808,15 @@ struct Decode {
                 s[tl][n][3] = v1 ? s[tl][n][3] * f1 : -INFINITY;
             }
         }
-        fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 4));
-        fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 8));
-        fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 16));
-        if (!(fv > 0.f)) fv = 1.f;
-        const float rF = rcp_approx(fv);
-        const float ratio = F * rF;
-        F = fv;
-#pragma unroll
-        for (int tl = 0; tl < NTL; ++tl) {
-            w0[tl] *= rF;
-            w1[tl] *= rF;
-        }
+        float ratio = 1.f;
+        if constexpr (kLazy)
+            softmax_step<NTL, true, true>(s, w0, w1, z0, z1, acc, m2, mt, ls, zs, F, rF);
+        else
+            ratio = eager_v_rebase<NTL>(w0, w1, F);
         uint32_t b[NTL][NT][2];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float mx = fmaxf(s[0][n][j], s[0][n][j + 2]);
-#pragma unroll
-                for (int tl = 1; tl < NTL; ++tl) mx = fmaxf(mx, fmaxf(s[tl][n][j], s[tl][n][j + 2]));
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-                const float mnew = fmaxf(m2[n][j], mx);
-                const float alpha = ex2(m2[n][j] - mnew);
-                m2[n][j] = mnew;
-                float sum = 0.f, zsum = 0.f;
-#pragma unroll
-                for (int tl = 0; tl < NTL; ++tl) {
-                    const float p0 = ex2(s[tl][n][j] - mnew), p1 = ex2(s[tl][n][j + 2] - mnew);
-                    sum += p0 + p1;
-                    zsum = fmaf(p0, z0[tl], fmaf(p1, z1[tl], zsum));
-                    s[tl][n][j] = p0 * w0[tl];
-                    s[tl][n][j + 2] = p1 * w1[tl];
-                }
-                ls[n][j] = ls[n][j] * alpha + sum;
-                zs[n][j] = zs[n][j] * alpha + zsum;
-                const float ar = alpha * ratio;
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    acc[n][m][j] *= ar;
-                    acc[n][m][j + 2] *= ar;
-                }
-            }
+            if constexpr (!kLazy) eager_rows<NTL, true, true>(n, s, w0, w1, z0, z1, acc, m2, ls, zs, ratio);
 #pragma unroll
             for (int tl = 0; tl < NTL; ++tl) {
                 b[tl][n][0] = movmatrix_trans(pack_f16(s[tl][n][0], s[tl][n][1]));
@@ -998,13 +1068,14 @@ struct Decode {
             if (has_next && (nx.b != cu.b || nx.h != cu.h)) load_q(a, nx, qn, lane);   // else: same rows
 
             float acc[NT][8][4];
-            float m2[NT][2], ls[NT][2], zs[NT][2];
-            float F = 1.f;
+            float m2[NT][2], mt[NT][2], ls[NT][2], zs[NT][2];
+            float F = 1.f, rF = 1.f;
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
 #pragma unroll
                 for (int m = 0; m < 8; ++m) acc[n][m][0] = acc[n][m][1] = acc[n][m][2] = acc[n][m][3] = 0.f;
                 m2[n][0] = m2[n][1] = -INFINITY;
+                mt[n][0] = mt[n][1] = -INFINITY;
                 ls[n][0] = ls[n][1] = 0.f;
                 zs[n][0] = zs[n][1] = 0.f;
             }
@@ -1030,14 +1101,14 @@ struct Decode {
                         const __half* const sc[2] = {
                             reinterpret_cast<const __half*>(smem + Cfg::kOffScales + s0 * Cfg::kScaleBytes),
                             reinterpret_cast<const __half*>(smem + Cfg::kOffScales + s1 * Cfg::kScaleBytes)};
-                        step_tq<2>(st, sc, vv, cq, lut, qf, acc, m2, ls, zs, F, lane);
+                        step_tq<2>(st, sc, vv, cq, lut, qf, acc, m2, mt, ls, zs, F, rF, lane);
                     } else if constexpr (FP8) {
                         const float* const sc[2] = {
                             reinterpret_cast<const float*>(smem + Cfg::kOffScales + s0 * Cfg::kScaleBytes),
                             reinterpret_cast<const float*>(smem + Cfg::kOffScales + s1 * Cfg::kScaleBytes)};
-                        step_fp8<2>(st, sc, vv, cq, qf, acc, m2, ls, F, lane);
+                        step_fp8<2>(st, sc, vv, cq, qf, acc, m2, mt, ls, F, rF, lane);
                     } else {
-                        step_bf16<2>(st, vv, a.qk_scale_log2, qf, acc, m2, ls, lane);
+                        step_bf16<2>(st, vv, a.qk_scale_log2, qf, acc, m2, mt, ls, lane);
                     }
                 } else {
                     const uint32_t st[1] = {sbase + Cfg::kOffStages + s0 * Cfg::kTileBytes};
@@ -1045,13 +1116,13 @@ struct Decode {
                     if constexpr (TQ) {
                         const __half* const sc[1] = {
                             reinterpret_cast<const __half*>(smem + Cfg::kOffScales + s0 * Cfg::kScaleBytes)};
-                        step_tq<1>(st, sc, vv, cq, lut, qf, acc, m2, ls, zs, F, lane);
+                        step_tq<1>(st, sc, vv, cq, lut, qf, acc, m2, mt, ls, zs, F, rF, lane);
                     } else if constexpr (FP8) {
                         const float* const sc[1] = {
                             reinterpret_cast<const float*>(smem + Cfg::kOffScales + s0 * Cfg::kScaleBytes)};
-                        step_fp8<1>(st, sc, vv, cq, qf, acc, m2, ls, F, lane);
+                        step_fp8<1>(st, sc, vv, cq, qf, acc, m2, mt, ls, F, rF, lane);
                     } else {
-                        step_bf16<1>(st, vv, a.qk_scale_log2, qf, acc, m2, ls, lane);
+                        step_bf16<1>(st, vv, a.qk_scale_log2, qf, acc, m2, mt, ls, lane);
                     }
                 }
                 __syncwarp();
@@ -1073,7 +1144,9 @@ struct Decode {
 
             // ---- epilogue: the last stage is free; stage the normalised partial through it
             // o = acc * F / l (F: the V-scale factor; TQ4 codes carry another 2^24, or 2^20 for the
-            // high nibbles), plus, for TQ4, the zero-point sum z / l
+            // high nibbles), plus, for TQ4, the zero-point sum z / l.  acc, l and z all count from
+            // the reference point m2; the stored statistics count from the true maximum M:
+            // m_p = M, l_p = l * 2^(m2 - M).
             float inv[NT][2], zq[NT][2];
 #pragma unroll
             for (int n = 0; n < NT; ++n)
@@ -1083,7 +1156,17 @@ struct Decode {
                     l += __shfl_xor_sync(kFull, l, 4);
                     l += __shfl_xor_sync(kFull, l, 8);
                     l += __shfl_xor_sync(kFull, l, 16);
-                    ls[n][j] = l;
+                    if constexpr (kLazy) {
+                        float M = mt[n][j];
+                        M = fmaxf(M, __shfl_xor_sync(kFull, M, 4));
+                        M = fmaxf(M, __shfl_xor_sync(kFull, M, 8));
+                        M = fmaxf(M, __shfl_xor_sync(kFull, M, 16));
+                        ls[n][j] = M == -INFINITY ? l : l * ex2(m2[n][j] - M);
+                        mt[n][j] = M;
+                    } else {
+                        ls[n][j] = l;
+                        mt[n][j] = m2[n][j];
+                    }
                     const float il = l > 0.f ? 1.f / l : 0.f;
                     inv[n][j] = il * (FP8 ? F : TQ ? F * 16777216.f : 1.f);
                     zq[n][j] = 0.f;
@@ -1147,7 +1230,7 @@ struct Decode {
                         const int q = n * 8 + 2 * tig + j;
                         if (q < a.QG) {
                             a.exp_sums[row0 + q] = ls[n][j];
-                            a.max_logits[row0 + q] = m2[n][j] * kLn2;
+                            a.max_logits[row0 + q] = mt[n][j] * kLn2;
                         }
                     }
             }
