@@ -594,15 +594,23 @@ struct Decode {
                 bl[tl][n][1] = movmatrix_trans(l23);
             }
         }
-        // V rows past the context may hold anything (NaN included): zero them, 0 * NaN = NaN.
-        uint32_t mlo[NTL], mhi[NTL];
-#pragma unroll
-        for (int tl = 0; tl < NTL; ++tl) {
-            mlo[tl] = mhi[tl] = kFull;
-            if (valid[tl] < kTileTokens) {
-                mlo[tl] = (2 * tig < valid[tl] ? 0x0000FFFFu : 0u) | (2 * tig + 1 < valid[tl] ? 0xFFFF0000u : 0u);
-                mhi[tl] = (2 * tig + 8 < valid[tl] ? 0x0000FFFFu : 0u) | (2 * tig + 9 < valid[tl] ? 0xFFFF0000u : 0u);
-            }
+        // Only a step's last tile can be partial (the one before it is followed by another); its
+        // V rows past the context may hold anything (NaN included) and are zeroed, 0 * NaN = NaN.
+        if (valid[NTL - 1] < kTileTokens)
+            pv_bf16<NTL, true>(st, valid, bh, bl, acc, lane);
+        else
+            pv_bf16<NTL, false>(st, valid, bh, bl, acc, lane);
+    }
+    template <int NTL, bool MASKED>
+    static __device__ __forceinline__ void pv_bf16(const uint32_t (&st)[NTL], const int (&valid)[NTL],
+                                                   const uint32_t (&bh)[NTL][NT][2], const uint32_t (&bl)[NTL][NT][2],
+                                                   float (&acc)[NT][8][4], int lane) {
+        const int tig = lane & 3;
+        uint32_t mlo = kFull, mhi = kFull;   // the last tile's token mask, 16 bits per token
+        if constexpr (MASKED) {
+            const int v = valid[NTL - 1];
+            mlo = (2 * tig < v ? 0x0000FFFFu : 0u) | (2 * tig + 1 < v ? 0xFFFF0000u : 0u);
+            mhi = (2 * tig + 8 < v ? 0x0000FFFFu : 0u) | (2 * tig + 9 < v ? 0xFFFF0000u : 0u);
         }
         const int vtok = (lane & 7) + ((lane >> 4) << 3), vhalf = (lane >> 3) & 1;
 #pragma unroll
@@ -613,10 +621,12 @@ struct Decode {
             for (int tl = 0; tl < NTL; ++tl) {
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4_trans(st[tl] + off, a0, a1, a2, a3);
-                a0 &= mlo[tl];
-                a1 &= mlo[tl];
-                a2 &= mhi[tl];
-                a3 &= mhi[tl];
+                if (MASKED && tl == NTL - 1) {
+                    a0 &= mlo;
+                    a1 &= mlo;
+                    a2 &= mhi;
+                    a3 &= mhi;
+                }
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
                     mma_bf16(acc[n][m], a0, a1, a2, a3, bh[tl][n][0], bh[tl][n][1]);
