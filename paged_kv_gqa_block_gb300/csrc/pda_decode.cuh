@@ -976,6 +976,17 @@ struct Decode {
         }
     }
 
+    // The fused step writes every output row.  A sequence with no tokens (context 0, or an invalid
+    // length, read as 0) has no unit, so its rows are zeroed here, as the reduce would; sequence b
+    // falls to CTA b mod grid.  Its context length was just read by find_range (L1-resident).
+    static __device__ void zero_empty_outputs(const DecodeArgs& a, int lane) {
+        const long long rows = (long long)a.Hk * a.QG;
+        for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
+            if (sanitize_ctx(__ldg(a.context_lens + b), a.MB * a.BS) != 0) continue;
+            for (long long r = 0; r < rows; ++r) store_out(a, (long long)b * rows + r, lane, make_float4(0.f, 0.f, 0.f, 0.f));
+        }
+    }
+
     // ------------------------------------------------------------------ the warp
     static __device__ void run(const DecodeArgs& a, const CUtensorMap* kv_map, const CUtensorMap* sc_map,
                                uint8_t* smem, uint32_t* tq_lut) {
@@ -995,6 +1006,7 @@ struct Decode {
         UnitIt cu;
         long long hi;
         find_range(a, cu, hi);
+        if constexpr (FUSED) zero_empty_outputs(a, lane);
         if (!(cu.b < a.B && cu.start < hi)) return;
 
         // Q rows and the first block-table entries are requested before anything waits

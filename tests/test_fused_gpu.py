@@ -50,6 +50,11 @@ CASES = [
     (wl.KV_BF16, 6, 32, 5, 3, (1281, 40, 3000)),
     (wl.KV_FP8_E4M3, 6, 16, 1, 2, (1, 300, 1100, 5000)),
     (wl.KV_FP8_E4M3, 16, 16, 1, 2, (16, 900)),
+    # empty sequences among others (their rows are zeroed, as the reduce does), and 79 partitions
+    # in one sequence (the in-kernel merge's path for more than 64)
+    (wl.KV_BF16, 8, 32, 1, 2, (20000, 0, 300, 0)),
+    (wl.KV_FP8_E4M3, 6, 32, 1, 1, (0, 18000, 5)),
+    (wl.KV_BF16, 8, 16, 1, 2, (0, 0, 0)),
 ]
 
 

@@ -122,6 +122,30 @@ def test_one_unit_per_warp(oracle_mod, kv):
     check_against_oracle(inp, res, oh.run_oracle(inp, partials=True))
 
 
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
+def test_more_than_64_partitions_and_empty_sequences(oracle_mod, kv):
+    # the longest sequence has 79 partitions of 256 tokens: the reduce holds (m_p, l_p) of 64
+    # partitions per row in registers and reloads the rest; empty sequences sit in between
+    ctx = (20000, 0, 16385, 300, 0, 1)
+    w = wl.small(num_seqs=6, num_kv_heads=2, query_group_size=8, kv_block_size=32, ctx=ctx, kv_dtype=kv, seed=71)
+    inp = wl.generate(w)
+    res = run_gpu(inp)
+    assert res["plan"].num_partitions == 79
+    check_against_oracle(inp, res, oh.run_oracle(inp, partials=True))
+    assert np.all(res["out"][[1, 4]] == 0) and np.all(res["out_bf16"][[1, 4]] == 0)
+
+
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
+def test_every_context_empty(oracle_mod, kv):
+    w = wl.small(num_seqs=3, num_kv_heads=2, ctx=(0, 0, 0), kv_dtype=kv, seed=72, max_blocks_per_seq=4)
+    inp = wl.generate(w)
+    res = run_gpu(inp)
+    assert res["err"] == 0
+    assert np.all(res["out"] == 0) and np.all(res["out_bf16"] == 0)
+    for key in ("part_o", "part_m", "part_l"):
+        assert is_sentinel(res[key]).all(), f"{key} was written"
+
+
 def test_key_bias_workload_small(oracle_mod):
     w = wl.small(num_seqs=3, num_kv_heads=2, query_group_size=16, kv_block_size=32, ctx=(2048, 2100, 3000),
                  seed=5, k_bias_std=2.0)
