@@ -74,6 +74,30 @@ def test_fused_matches_oracle_and_the_two_launch_path(oracle_mod, pda, kv, QG, B
             assert np.all(np.abs(o - ref) <= tol + bf16_half_ulp(ref))
 
 
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
+def test_fused_bad_context_length_sets_the_bit_and_zeroes_that_sequence(oracle_mod, pda, kv):
+    w = wl.small(num_seqs=3, num_kv_heads=2, ctx=(300, 20, 33), kv_dtype=kv, seed=38)
+    inp = wl.generate(w)
+    ref = oh.run_oracle(inp)["out"]
+    ctx = inp.context_lens.copy()
+    ctx[1] = -5
+    d = to_device(wl.Inputs(w, inp.query, inp.cache, inp.block_table, ctx))
+    p = plan_for(w)
+    ws = pda.workspace(p, "cuda")
+    cnt = pda.counters(p, "cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = torch.full((w.num_seqs, w.num_q_heads, 128), float("nan"), dtype=torch.float32, device="cuda")
+    pda.decode_fused(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"],
+                     ws["partial_out"], ws["exp_sums"], ws["max_logits"], cnt, o, err_word=err)
+    torch.cuda.synchronize()
+    out = o.cpu().numpy().astype(np.float64)
+    assert int(err.item()) & 1
+    assert np.all(out[1] == 0)
+    for b in (0, 2):
+        assert np.abs(out[b] - ref[b]).max() <= TOL[kv]
+    assert int(cnt.abs().sum().item()) == 0
+
+
 @pytest.mark.parametrize("name", ["b8_hk8_qg8_bs16_ctx1-4096", "b64_hk8_qg6_bs16_fp8_lognormal2048"])
 def test_fused_full_size_equals_two_launch(pda, name):
     inp = wl.generate(wl.WORKLOADS[name])
