@@ -455,6 +455,7 @@ def run_ours(args, rank, world, local_rank):
                    "tile_groups_per_partition": p.resolved_tile_groups, "num_partitions": p.num_partitions,
                    "context_tokens": ab["tokens"], "seq_len_max": int(inp.context_lens.max()),
                    "parallelism": f"replicas{world}", "l2": "flushed between timed steps (512 MiB write, then 256 MiB read)"},
+        "query_head_steps_per_s": replica_throughput(world, B_units * w.query_group_size, mean_step),
         "kv_read_gbs": kv_gbs * world,
         "kv_read_frac_of_8tbs": kv_gbs / NOMINAL_HBM_GBS,
         "kv_read_frac_of_measured": kv_gbs / peak,
