@@ -199,7 +199,9 @@ PDA_API int pda_append_kv(const pda_plan_t* plan, const void* k_new, const void*
  * reduce of pda_reduce performed inside the same launch by the last partition of each
  * (sequence, KV head) to finish (the split-reduce pattern of "last arrival sums in order";
  * nothing waits).  A (sequence, KV head) whose context fits one partition is written to `out`
- * directly (its partial is not stored).  The combination is the one pda_reduce computes, in
+ * directly (its partial is not stored); the rows of a sequence with no tokens (context 0, or an
+ * invalid length, which also sets PDA_ERRW_BAD_CONTEXT_LEN) are written as zeros, as pda_reduce
+ * writes them.  The combination is the one pda_reduce computes, in
  * partition order, so results are deterministic and equal pda_decode + pda_reduce's.
  *   partial_out, exp_sums, max_logits   as for pda_decode (scratch here)
  *   counters   device int32 [B][Hk]: must be zero before the first call; every completed call
