@@ -1048,11 +1048,19 @@ struct Decode {
         int cs = 0;                          // next stage to consume and its barrier phase
         uint32_t cph = 0;
         bool ok = true;
+        // Q fragments of the current unit.  The f16 kernels with QG <= 8 rebuild them only when the
+        // unit's (sequence, head) differs from the previous unit's (consecutive partitions of one
+        // head share their Q rows; the conversion to f16 costs ~0.6 us of a warp per unit).  The
+        // others rebuild them every unit: keeping them across the epilogue costs registers (QG = 16
+        // measured 5 % slower), and for bf16 they are plain register moves.
+        constexpr bool kKeepQ = F16 && NT == 1;
+        uint32_t qf[NT][8][2];
+        float cq = a.qk_scale_log2;
+        bool new_q = true;
         while (ok) {
             // ---- unit start: Q fragments, next unit's Q in flight
-            uint32_t qf[NT][8][2];
-            float cq = a.qk_scale_log2;
-            if constexpr (!F16) {
+            if (!new_q) {
+            } else if constexpr (!F16) {
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -1087,7 +1095,9 @@ struct Decode {
             UnitIt nx = cu;
             it_advance(nx, a);
             const bool has_next = nx.b < a.B && nx.start < hi;
-            if (has_next && (nx.b != cu.b || nx.h != cu.h)) load_q(a, nx, qn, lane);   // else: same rows
+            const bool other_rows = nx.b != cu.b || nx.h != cu.h;
+            if (has_next && other_rows) load_q(a, nx, qn, lane);   // else: same rows
+            new_q = !kKeepQ || (has_next && other_rows);
 
             float acc[NT][8][4];
             float m2[NT][2], mt[NT][2], ls[NT][2], zs[NT][2];
@@ -1214,19 +1224,34 @@ struct Decode {
                 for (int n = 0; n < NT; ++n) {
                     if (n * 8 + 8 <= r0 || n * 8 >= r0 + kPassRows) continue;
 #pragma unroll
-                    for (int m = 0; m < 8; ++m)
+                    for (int m = 0; m < 8; ++m) {
+                        if constexpr (F16) {
+                            // elements c and c + 2 are dimensions d and d + 1 of one row: one 8-byte store
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const int ql = n * 8 + 2 * tig + (c & 1) - r0;
-                            if (ql < 0 || ql >= kPassRows) continue;   // a pass of 4 rows holds half an n-tile
-                            const int d = TQ    ? (32 * (m >> 1) + 4 * gid + 2 * (m & 1) + (c >> 1))
-                                          : F16 ? (16 * gid + 2 * m + (c >> 1))
-                                                : (16 * m + gid + 8 * (c >> 1));
-                            float v = acc[n][m][c] * inv[n][c & 1];
-                            if constexpr (TQ) v = fmaf(acc[n][m][c], (c >> 1) ? inv[n][c & 1] * 0.0625f : inv[n][c & 1],
-                                                       zq[n][c & 1]);
-                            stg[ql * kHeadDim + ((((d >> 2) ^ (ql & 6))) << 2) + (d & 3)] = v;
+                            for (int j = 0; j < 2; ++j) {
+                                const int ql = n * 8 + 2 * tig + j - r0;
+                                if (ql < 0 || ql >= kPassRows) continue;   // a pass of 4 rows holds half an n-tile
+                                const int d = TQ ? (32 * (m >> 1) + 4 * gid + 2 * (m & 1)) : (16 * gid + 2 * m);
+                                float2 v;
+                                if constexpr (TQ) {
+                                    v.x = fmaf(acc[n][m][j], inv[n][j], zq[n][j]);
+                                    v.y = fmaf(acc[n][m][j + 2], inv[n][j] * 0.0625f, zq[n][j]);
+                                } else {
+                                    v.x = acc[n][m][j] * inv[n][j];
+                                    v.y = acc[n][m][j + 2] * inv[n][j];
+                                }
+                                *reinterpret_cast<float2*>(stg + ql * kHeadDim + ((((d >> 2) ^ (ql & 6))) << 2) + (d & 3)) = v;
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const int ql = n * 8 + 2 * tig + (c & 1) - r0;
+                                if (ql < 0 || ql >= kPassRows) continue;
+                                const int d = 16 * m + gid + 8 * (c >> 1);
+                                stg[ql * kHeadDim + ((((d >> 2) ^ (ql & 6))) << 2) + (d & 3)] = acc[n][m][c] * inv[n][c & 1];
+                            }
                         }
+                    }
                 }
                 __syncwarp();
                 const int rows = min(kPassRows, a.QG - r0);
