@@ -109,6 +109,22 @@ def test_more_units_than_warps(oracle_mod, kv):
 
 
 @pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
+def test_large_batch_of_short_contexts(oracle_mod, kv):
+    # 1500 sequences: every lane of the work scan walks 47 of them; contexts 0-300 tokens (one or
+    # two partitions, some empty), sampled units checked against the oracle with their partials
+    rng = np.random.default_rng(13)
+    ctx = tuple(int(c) for c in rng.integers(0, 301, size=1500))
+    w = wl.small(num_seqs=1500, num_kv_heads=2, query_group_size=8, kv_block_size=16, ctx=ctx, kv_dtype=kv, seed=43,
+                 max_blocks_per_seq=19)
+    inp = wl.generate(w)
+    res = run_gpu(inp)
+    units = np.sort(rng.choice(1500 * 2, size=200, replace=False))
+    check_against_oracle(inp, res, oh.run_oracle(inp, partials=True, units=units), units=units)
+    empty = [b for b, c in enumerate(ctx) if c == 0]
+    assert empty and np.all(res["out"][empty] == 0)
+
+
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
 def test_one_unit_per_warp(oracle_mod, kv):
     # room for 16 x 8 x 16 = 2048 partitions (more than the grid's warps) but short contexts
     # give at most 16 x 8 x 3 = 384 non-empty ones: each warp takes one whole unit
