@@ -1,5 +1,5 @@
 // pda_ptx.cuh -- thin inline-PTX wrappers used by the sm_103a kernels of libpda.
-// mbarrier phases, TMA (cp.async.bulk.tensor / cp.async.bulk) into shared memory, warp-level
+// mbarrier phases, TMA tensor copies (cp.async.bulk.tensor) into shared memory, warp-level
 // tensor-core fragments (ldmatrix, mma.sync, movmatrix) and the few conversions the kernels need.
 #pragma once
 
@@ -23,9 +23,6 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 // Suspends until the phase completes or a time limit of the hardware's passes; true if it
 // completed.
@@ -104,12 +101,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
         "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
         : "memory");
 }
-// Contiguous bulk copy (both addresses 16-byte aligned, bytes a multiple of 16).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
 
 // ------------------------------------------------------------------ warp-level MMA fragments
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -125,9 +116,6 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
 }
 __device__ __forceinline__ void lds128(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-__device__ __forceinline__ void lds64(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 // D(16x8, f32) += A(16x16, row) * B(16x8, col)
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
