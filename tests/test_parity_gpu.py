@@ -125,6 +125,19 @@ def test_large_batch_of_short_contexts(oracle_mod, kv):
 
 
 @pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
+def test_many_kv_heads(oracle_mod, kv):
+    # 32 KV heads of QG 6 (192 query heads): the head dimension of the tensor maps and the
+    # per-head metadata offsets at a large head count; 1056 units (tile-balanced on the 912-warp
+    # bf16 grid, one unit per warp on the 1824-warp fp8 and TQ4 grids)
+    ctx = (4000, 1, 1300, 700, 256, 1500)
+    w = wl.small(num_seqs=6, num_kv_heads=32, query_group_size=6, kv_block_size=16, ctx=ctx, kv_dtype=kv, seed=44)
+    inp = wl.generate(w)
+    res = run_gpu(inp)
+    units = np.sort(np.random.default_rng(3).choice(6 * 32, size=48, replace=False))
+    check_against_oracle(inp, res, oh.run_oracle(inp, partials=True, units=units), units=units)
+
+
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
 def test_one_unit_per_warp(oracle_mod, kv):
     # room for 16 x 8 x 16 = 2048 partitions (more than the grid's warps) but short contexts
     # give at most 16 x 8 x 3 = 384 non-empty ones: each warp takes one whole unit
