@@ -1,5 +1,6 @@
 """The seeded generator: determinism, layout, poison and the fp8 scale convention (no GPU)."""
 import numpy as np
+import pytest
 import torch
 
 from paged_kv_gqa_block_gb300 import workloads as wl
@@ -87,3 +88,34 @@ def test_bf16_rounding_is_nearest_even():
     ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
     assert np.array_equal(wl.bf16_bits_to_f32(wl.round_bf16(x)), ref)
     assert wl.bf16_bits_to_f32(wl.round_bf16(np.float32(1.0 + 2 ** -8)))[()] == 1.0
+
+
+# The input recipe of every workload, as the design notes state it: shapes, pool size, context
+# range, tables drawn without replacement from the pool, the key-bias spread, seeds 1001..1006.
+RECIPES = {
+    # name: (B, Hk, QG, BS, MB, pool, kv dtype, ctx kind, lo, hi, k_bias_std, seed)
+    "b1_hk1_qg8_bs16_ctx256": (1, 1, 8, 16, 16, 64, wl.KV_BF16, "fixed", 256, 256, 0.0, 1001),
+    "b8_hk8_qg8_bs16_ctx1-4096": (8, 8, 8, 16, 256, 2048, wl.KV_BF16, "uniform", 1, 4096, 0.0, 1002),
+    "b32_hk4_qg16_bs32_ctx2048-8192_kbias": (32, 4, 16, 32, 256, 8192, wl.KV_BF16, "uniform", 2048, 8192, 2.0, 1003),
+    "b4_hk8_qg8_bs32_ctx32768_g5p32": (4, 8, 8, 32, 1280, 5120, wl.KV_BF16, "fixed", 32768, 32768, 0.0, 1004),
+    "b64_hk8_qg6_bs16_fp8_lognormal2048": (64, 8, 6, 16, 1024, 65536, wl.KV_FP8_E4M3, "lognormal", 16, 16384, 0.0, 1005),
+    "b64_hk8_qg6_bs16_tq4_lognormal2048": (64, 8, 6, 16, 1024, 65536, wl.KV_TQ4, "lognormal", 16, 16384, 0.0, 1006),
+}
+
+
+@pytest.mark.parametrize("name", sorted(RECIPES))
+def test_every_workload_follows_its_recipe(name):
+    B, Hk, QG, BS, MB, pool, kv, kind, lo, hi, kb, seed = RECIPES[name]
+    w = wl.WORKLOADS[name]
+    assert (w.num_seqs, w.num_kv_heads, w.query_group_size, w.kv_block_size, w.max_blocks_per_seq) == (B, Hk, QG, BS, MB)
+    assert (w.num_cache_blocks, w.kv_dtype, w.ctx[0], w.k_bias_std, w.seed) == (pool, kv, kind, kb, seed)
+    rng = np.random.Generator(np.random.PCG64(w.seed))    # the generator's own draw order: lengths, then tables
+    ctx = wl.draw_context_lens(w, rng)
+    table = wl.draw_block_table(w, rng)
+    assert ctx.min() >= lo and ctx.max() <= hi and ctx.max() <= MB * BS
+    assert table.shape == (B, MB) and table.min() >= 0 and table.max() < pool
+    assert len(np.unique(table)) == table.size               # without replacement
+    if kind == "uniform":                                     # both ends reachable, spread over the range
+        assert ctx.max() - ctx.min() > (hi - lo) // 2
+    if kind == "lognormal":                                   # median near exp(mu) = 2048, the clip respected
+        assert 1200 < np.median(ctx) < 3500
