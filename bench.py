@@ -101,7 +101,7 @@ def algorithmic_bytes(w: wl.Workload, ctx: np.ndarray, W: int) -> dict:
     bt = int(np.sum(-(-ctx.astype(np.int64) // w.kv_block_size))) * 4
     partials = nvalid * Hk * QG * (D * 4 + 8)
     out = w.num_seqs * Hk * QG * D * 2
-    return {"kv": kv, "decode": kv + q + bt + 4 * w.num_seqs + partials, "reduce": 2 * partials + out,
+    return {"kv": kv, "decode": kv + q + bt + 4 * w.num_seqs + partials, "reduce": partials + out,
             "tokens": tok, "units": w.num_seqs * Hk}
 
 
