@@ -2,7 +2,10 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-Prints one JSON line (rank 0).  A step is one pass of the whole hot path over one batch:
+Prints one JSON line (rank 0).  The headline workload is the largest configuration, the long
+context (4 sequences of 32 768 tokens, 8 KV heads, QG 8, 32-token blocks, 32 partitions of 1280
+tokens); the line's "other_workloads" list times every other configuration the same way in the
+same run (the fp8 one among them).  A step is one pass of the whole hot path over one batch:
 pda_decode (the partition kernel) then pda_reduce, both through the C ABI, inputs resident in
 HBM.  Between timed steps, outside the timed events, L2 is flushed: a 512 MiB write, then a
 256 MiB read of another buffer, so that the step starts with an L2 holding none of its inputs
@@ -34,7 +37,8 @@ sys.path.insert(0, ROOT)
 
 from paged_kv_gqa_block_gb300 import workloads as wl   # noqa: E402
 
-DEFAULT_WORKLOAD = wl.WORKLOAD_ORDER[1]
+# the headline: the largest configuration (the long-context one, 537 MB of KV per step)
+DEFAULT_WORKLOAD = "b4_hk8_qg8_bs32_ctx32768_g5p32"
 METRIC = "decode seq-head-steps/s and KV-read HBM GB/s (fraction of ~8 TB/s), 1 GB300"
 UNIT = "seq-head-steps/s"
 NOMINAL_HBM_GBS = 8000.0
@@ -58,6 +62,8 @@ def parse():
     ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="time only --workload (by default the other configurations are timed too)")
     return ap.parse_args()
 
 
@@ -264,6 +270,107 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------------------------ our leg
+class _Step:
+    """One workload resident on the device: inputs, plan, workspace, and the calls of one step."""
+
+    def __init__(self, pda, w, inp, dev, stream, path):
+        import torch
+        self.w, self.inp, self.path, self.stream, self.pda = w, inp, path, stream, pda
+        self.p = pda.plan(w.num_seqs, w.num_kv_heads, w.query_group_size, w.kv_block_size, w.max_blocks_per_seq,
+                          w.tile_groups_per_partition, w.max_partitions, w.kv_dtype, w.softmax_scale)
+        # the step's per-call inputs (query, block table, context lengths) live in one device buffer,
+        # so that the end-to-end loop moves them from host memory with a single copy
+        parts = [inp.query.view(np.uint8).reshape(-1), inp.block_table.view(np.uint8).reshape(-1),
+                 inp.context_lens.view(np.uint8).reshape(-1)]
+        offs, total = [], 0
+        for x in parts:
+            offs.append(total)
+            total += (x.size + 255) // 256 * 256
+        self.step_in_host = torch.zeros(total, dtype=torch.uint8).pin_memory()
+        for x, o in zip(parts, offs):
+            self.step_in_host[o:o + x.size] = torch.from_numpy(x)
+        self.step_in = self.step_in_host.to(dev)
+
+        def views(buf):
+            return (buf[offs[0]:offs[0] + parts[0].size].view(torch.bfloat16).view(inp.query.shape),
+                    buf[offs[1]:offs[1] + parts[1].size].view(torch.int32).view(inp.block_table.shape),
+                    buf[offs[2]:offs[2] + parts[2].size].view(torch.int32))
+        self.q, self.bt, self.ctx = views(self.step_in)
+        self.qh, self.bth, self.ctxh = views(self.step_in_host)
+        self.cache = torch.from_numpy(inp.cache).to(dev)
+        self.tq4 = w.kv_dtype == wl.KV_TQ4
+        self.cent = torch.from_numpy(inp.extra["centroids"]).to(dev) if self.tq4 else None
+        if self.tq4 and path == "fused":
+            raise SystemExit("the fused step does not read TQ4 caches; use --path two")
+        self.ws = pda.workspace(self.p, dev)
+        self.out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+        self.outh = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.cnt = pda.counters(self.p, dev)
+        self.launches_per_step = 1 if path == "fused" else 2
+        self.units = w.num_seqs * w.num_kv_heads
+
+    def decode_on(self, qx, btx, ctxx):
+        w, ws, pda = self.w, self.ws, self.pda
+        if self.tq4:
+            pda.decode_tq4(self.p, qx, self.cache, w.num_cache_blocks, self.cent, btx, ctxx, ws["partial_out"],
+                           ws["exp_sums"], ws["max_logits"], err_word=self.err, stream=self.stream)
+        else:
+            pda.decode(self.p, qx, self.cache, w.num_cache_blocks, btx, ctxx, ws["partial_out"], ws["exp_sums"],
+                       ws["max_logits"], err_word=self.err, stream=self.stream)
+
+    def step_on(self, qx, btx, ctxx, outx):
+        w, ws, pda = self.w, self.ws, self.pda
+        if self.path == "fused":
+            pda.decode_fused(self.p, qx, self.cache, w.num_cache_blocks, btx, ctxx, ws["partial_out"],
+                             ws["exp_sums"], ws["max_logits"], self.cnt, outx, err_word=self.err, stream=self.stream)
+        else:
+            self.decode_on(qx, btx, ctxx)
+            pda.reduce(self.p, ctxx, ws["partial_out"], ws["exp_sums"], ws["max_logits"], outx, err_word=self.err,
+                       stream=self.stream)
+
+    def step(self):
+        self.step_on(self.q, self.bt, self.ctx, self.out)
+
+    def decode(self):
+        self.decode_on(self.q, self.bt, self.ctx)
+
+    def check_err(self):
+        if int(self.err.item()) != 0:
+            raise RuntimeError(f"{self.w.name}: device error word {int(self.err.item())}")
+
+
+def event_times(fn, n, flush, stream, before=None):
+    """Device time of `fn` on `stream` for n calls (CUDA events on that stream, L2 flushed before
+    each call outside the events); seconds."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush()
+        a, b = ev[i]
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e-3 for a, b in ev]
+
+
+def rates(w, inp, p, mean_step, mean_dec, world, peak, peaks):
+    ab = algorithmic_bytes(w, inp.context_lens, p.partition_tokens)
+    achieved = ab["decode"] / mean_dec / 1e9
+    kv_gbs = ab["kv"] / mean_step / 1e9
+    return ab, {
+        "kv_read_gbs": kv_gbs * world,
+        "kv_read_frac_of_8tbs": kv_gbs / NOMINAL_HBM_GBS,
+        "kv_read_frac_of_measured": kv_gbs / peak,
+        "decode_ms": mean_dec * 1e3,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": committed_traffic(w.name), "kernel": "pda_partition_kernel",
+                     "algorithmic_bytes_per_launch": ab["decode"],
+                     "peak_source": "measured" if peaks else "fallback"},
+    }
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import paged_kv_gqa_block_gb300 as pda
@@ -278,117 +385,50 @@ def run_ours(args, rank, world, local_rank):
 
     w = wl.WORKLOADS[args.workload]
     inp = wl.generate(w)
-    p = pda.plan(w.num_seqs, w.num_kv_heads, w.query_group_size, w.kv_block_size, w.max_blocks_per_seq,
-                 w.tile_groups_per_partition, w.max_partitions, w.kv_dtype, w.softmax_scale)
-    # the step's per-call inputs (query, block table, context lengths) live in one device buffer,
-    # so that the end-to-end loop moves them from host memory with a single copy
-    parts = [inp.query.view(np.uint8).reshape(-1), inp.block_table.view(np.uint8).reshape(-1),
-             inp.context_lens.view(np.uint8).reshape(-1)]
-    offs, total = [], 0
-    for x in parts:
-        offs.append(total)
-        total += (x.size + 255) // 256 * 256
-    step_in_host = torch.zeros(total, dtype=torch.uint8).pin_memory()
-    for x, o in zip(parts, offs):
-        step_in_host[o:o + x.size] = torch.from_numpy(x)
-    step_in = step_in_host.to(dev)
-    q = step_in[offs[0]:offs[0] + parts[0].size].view(torch.bfloat16).view(inp.query.shape)
-    bt = step_in[offs[1]:offs[1] + parts[1].size].view(torch.int32).view(inp.block_table.shape)
-    ctx = step_in[offs[2]:offs[2] + parts[2].size].view(torch.int32)
-    cache = torch.from_numpy(inp.cache).to(dev)
-    tq4 = w.kv_dtype == wl.KV_TQ4
-    cent = torch.from_numpy(inp.extra["centroids"]).to(dev) if tq4 else None
-    if tq4 and args.path == "fused":
-        raise SystemExit("the fused step does not read TQ4 caches; use --path two")
-    ws = pda.workspace(p, dev)
-    out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean_buf = torch.zeros(L2_CLEAN_READ_BYTES // 4, dtype=torch.float32, device=dev)
 
-    class _Flush:
-        @staticmethod
-        def zero_():
-            flush_buf.zero_()       # evicts everything from L2 ...
-            clean_buf.sum()         # ... and leaves it holding clean lines of another buffer
-    flush = _Flush()
+    def flush():
+        flush_buf.zero_()       # evicts everything from L2 ...
+        clean_buf.sum()         # ... and leaves it holding clean lines of another buffer
     if args.graph:      # graphs are captured on a non-default stream: run everything on one
         torch.cuda.set_stream(torch.cuda.Stream(dev))
     stream = torch.cuda.current_stream(dev)
-    B_units = w.num_seqs * w.num_kv_heads
-
-    cnt = pda.counters(p, dev)
-    launches_per_step = 1 if args.path == "fused" else 2
-
-    def decode_on(qx, btx, ctxx):
-        if tq4:
-            pda.decode_tq4(p, qx, cache, w.num_cache_blocks, cent, btx, ctxx, ws["partial_out"], ws["exp_sums"],
-                           ws["max_logits"], err_word=err, stream=stream)
-        else:
-            pda.decode(p, qx, cache, w.num_cache_blocks, btx, ctxx, ws["partial_out"], ws["exp_sums"],
-                       ws["max_logits"], err_word=err, stream=stream)
-
-    def step_on(qx, btx, ctxx, outx):
-        if args.path == "fused":
-            pda.decode_fused(p, qx, cache, w.num_cache_blocks, btx, ctxx, ws["partial_out"], ws["exp_sums"],
-                             ws["max_logits"], cnt, outx, err_word=err, stream=stream)
-        else:
-            decode_on(qx, btx, ctxx)
-            pda.reduce(p, ctxx, ws["partial_out"], ws["exp_sums"], ws["max_logits"], outx, err_word=err, stream=stream)
-
-    def step():
-        step_on(q, bt, ctx, out)
+    S = _Step(pda, w, inp, dev, stream, args.path)
+    step = S.step
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     if args.graph:      # capture one step; the timed loops replay it
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
-            step()
+            S.step()
         torch.cuda.synchronize()
-        step_direct = step
 
         def step():
             graph.replay()
         for _ in range(3):
-            flush.zero_()
+            flush()
             step()
         torch.cuda.synchronize()
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error word {int(err.item())}")
+    S.check_err()
 
     # ---- device-resident timing: events around each whole step on the launching stream (nothing
     # between the two launches, so the reduce can be scheduled while the partition pass drains)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
         wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()
-            a, b = ev[i]
-            a.record(stream)
-            step()
-            b.record(stream)
-        torch.cuda.synchronize()
+        t_step = event_times(step, args.steps, flush, stream)
         wall = time.perf_counter() - wall0
     if dist:
         dist.barrier()
-    t_step = [a.elapsed_time(b) * 1e-3 for a, b in ev]
     # the partition kernel alone (roofline of the dominant kernel)
     dec_steps = max(20, min(args.steps, 500))
-    evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(dec_steps)]
-    for i in range(dec_steps):
-        flush.zero_()
-        a, b = evd[i]
-        a.record(stream)
-        decode_on(q, bt, ctx)
-        b.record(stream)
-    torch.cuda.synchronize()
-    t_dec = [a.elapsed_time(b) * 1e-3 for a, b in evd]
+    t_dec = event_times(S.decode, dec_steps, flush, stream)
     mean_step, mean_dec = sum(t_step) / len(t_step), sum(t_dec) / len(t_dec)
     med_step, min_step = float(np.median(t_step)), min(t_step)
     if dist:
@@ -399,30 +439,26 @@ def run_ours(args, rank, world, local_rank):
     # memory, which the kernels read and write across the host link.  Beside it: the same step
     # with one explicit copy of the packed inputs in and one of the output out.  The KV cache is
     # device-resident state in both.
-    outh = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
     e2e_steps = max(10, min(args.steps, 500))
     e2e = []
     for i in range(e2e_steps + 3):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        step_in.copy_(step_in_host, non_blocking=True)
+        S.step_in.copy_(S.step_in_host, non_blocking=True)
         step()
-        outh.copy_(out, non_blocking=True)
+        S.outh.copy_(S.out, non_blocking=True)
         b.record(stream)
         b.synchronize()
         if i >= 3:
             e2e.append(a.elapsed_time(b) * 1e-3)
     mean_e2e = sum(e2e) / len(e2e)
-    qh = step_in_host[offs[0]:offs[0] + parts[0].size].view(torch.bfloat16).view(inp.query.shape)
-    bth = step_in_host[offs[1]:offs[1] + parts[1].size].view(torch.int32).view(inp.block_table.shape)
-    ctxh = step_in_host[offs[2]:offs[2] + parts[2].size].view(torch.int32)
     e2e_zc = []
     for i in range(e2e_steps + 3):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        step_on(qh, bth, ctxh, outh)
+        S.step_on(S.qh, S.bth, S.ctxh, S.outh)
         b.record(stream)
         b.synchronize()
         if i >= 3:
@@ -431,22 +467,53 @@ def run_ours(args, rank, world, local_rank):
     if dist:
         mean_e2e, mean_e2e_zc = max_over_ranks(dist, [mean_e2e, mean_e2e_zc], dev)
     torch.cuda.synchronize()
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error word {int(err.item())}")
+    S.check_err()
+
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks and peaks.get("hbm_gbs") else FALLBACK_HBM_GBS
+    p = S.p
+    units = S.units
+
+    # ---- the other configurations, timed the same way in the same run (device-resident inputs,
+    # L2 flushed between steps); each is generated, timed and freed in turn
+    others = []
+    if not args.no_other_workloads:
+        del S
+        n_other = max(50, min(args.steps, 500))
+        for name in wl.WORKLOAD_ORDER:
+            if name == w.name:
+                continue
+            wo = wl.WORKLOADS[name]
+            io = wl.generate(wo)
+            So = _Step(pda, wo, io, dev, stream, "two")
+            for _ in range(max(3, args.warmup)):
+                flush()
+                So.step()
+            torch.cuda.synchronize()
+            So.check_err()
+            ts = event_times(So.step, n_other, flush, stream)
+            td = event_times(So.decode, n_other, flush, stream)
+            So.check_err()
+            ms, md = sum(ts) / len(ts), sum(td) / len(td)
+            if dist:
+                ms, md = max_over_ranks(dist, [ms, md], dev)
+            _, r = rates(wo, io, So.p, ms, md, world, peak, peaks)
+            others.append({"workload": name, "kv_dtype": KV_NAMES[wo.kv_dtype], "steps": n_other,
+                           "value": replica_throughput(world, So.units, ms), "unit": UNIT,
+                           "ms_per_step": ms * 1e3, "step_ms_median": float(np.median(ts)) * 1e3, **r})
+            del So, io
+            torch.cuda.empty_cache()
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
 
-    ab = algorithmic_bytes(w, inp.context_lens, p.partition_tokens)
-    peaks = measured_peaks()
-    peak = peaks["hbm_gbs"] if peaks and peaks.get("hbm_gbs") else FALLBACK_HBM_GBS
-    achieved = ab["decode"] / mean_dec / 1e9
-    kv_gbs = ab["kv"] / mean_step / 1e9
+    ab, r = rates(w, inp, p, mean_step, mean_dec, world, peak, peaks)
     res = {
-        "metric": METRIC, "value": replica_throughput(world, B_units, mean_step), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_step * 1e3, "higher_is_better": True,
-        "step_ms_median": med_step * 1e3, "step_ms_min": min_step * 1e3,
+        "metric": METRIC, "value": replica_throughput(world, units, mean_step), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_step * 1e3,
+        "higher_is_better": True, "step_ms_median": med_step * 1e3, "step_ms_min": min_step * 1e3,
         "scaling": "weak", "vs_baseline": None,
         "dtype": KV_NAMES[w.kv_dtype],
         "data": "synthetic",
@@ -455,30 +522,25 @@ def run_ours(args, rank, world, local_rank):
                    "tile_groups_per_partition": p.resolved_tile_groups, "num_partitions": p.num_partitions,
                    "context_tokens": ab["tokens"], "seq_len_max": int(inp.context_lens.max()),
                    "parallelism": f"replicas{world}", "l2": "flushed between timed steps (512 MiB write, then 256 MiB read)"},
-        "query_head_steps_per_s": replica_throughput(world, B_units * w.query_group_size, mean_step),
-        "kv_read_gbs": kv_gbs * world,
-        "kv_read_frac_of_8tbs": kv_gbs / NOMINAL_HBM_GBS,
-        "kv_read_frac_of_measured": kv_gbs / peak,
-        "decode_ms": mean_dec * 1e3,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": committed_traffic(w.name), "kernel": "pda_partition_kernel",
-                     "algorithmic_bytes_per_launch": ab["decode"],
-                     "peak_source": "measured" if peaks else "fallback"},
-        "e2e": {"value": replica_throughput(world, B_units, mean_e2e_zc), "unit": UNIT,
-                "h2d_bytes_per_step": int(qh.numel() * 2 + bth.numel() * 4 + ctxh.numel() * 4),
-                "d2h_bytes_per_step": int(outh.numel() * 2),
+        "query_head_steps_per_s": replica_throughput(world, units * w.query_group_size, mean_step),
+        **r,
+        "e2e": {"value": replica_throughput(world, units, mean_e2e_zc), "unit": UNIT,
+                "h2d_bytes_per_step": int(inp.query.nbytes + inp.block_table.nbytes + inp.context_lens.nbytes),
+                "d2h_bytes_per_step": int(w.num_seqs * w.num_q_heads * w.head_dim * 2),
                 "how": "inputs and output in pinned host memory, read and written by the kernels"},
-        "e2e_with_copies": {"value": replica_throughput(world, B_units, mean_e2e), "unit": UNIT,
-                            "h2d_bytes_per_step": int(step_in_host.numel()),
-                            "d2h_bytes_per_step": int(outh.numel() * 2),
+        "e2e_with_copies": {"value": replica_throughput(world, units, mean_e2e), "unit": UNIT,
+                            "h2d_bytes_per_step": int(e2e_in_bytes(inp)),
+                            "d2h_bytes_per_step": int(w.num_seqs * w.num_q_heads * w.head_dim * 2),
                             "how": "one copy of the packed inputs in, one copy of the output out"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": (1 if args.path == "fused" else 2) * args.steps,
         "step_path": ("pda_decode_fused (one launch)" if args.path == "fused" else "pda_decode + pda_reduce") +
                      (", replayed from a CUDA graph" if args.graph else ""),
         "decode_launches_timed_separately": dec_steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
     }
+    if others:
+        res["other_workloads"] = others
     if not args.no_cpu_baseline and world >= 1:
         v, threads, sample = oracle_units_per_s(inp, args.cpu_budget_s)
         res["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
@@ -487,6 +549,11 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(res))
     if dist:
         dist.destroy_process_group()
+
+
+def e2e_in_bytes(inp) -> int:
+    """Bytes of the packed per-step inputs copied in by the end-to-end loop (each part padded to 256)."""
+    return sum((x.nbytes + 255) // 256 * 256 for x in (inp.query, inp.block_table, inp.context_lens))
 
 
 def main():

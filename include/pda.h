@@ -230,8 +230,12 @@ PDA_API int pda_decode_fused(const pda_plan_t* plan, const void* query, const vo
  * The array holds PDA_NOALLOC_SCRATCH_BYTES (64 MiB) on every GPU that loads the library, until
  * the process exits.  A plan whose partials (B*Hk*P*QG*(D*4 + 8) bytes, each part rounded up to
  * 256 bytes) do not fit returns PDA_ERR_WORKSPACE_TOO_SMALL and launches nothing.
+ * query, block_table, context_lens and out may be pinned host memory, as for pda_decode and
+ * pda_reduce.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  The call allocates
+ * that device current; make that first call before any stream capture.  The address is kept for
+ * the life of the process: after cudaDeviceReset, or anything else that destroys the device's
+ * primary context, do not call this entry point again in the same process.  The call allocates
  * nothing and frees nothing.
  * All calls share the one array and it keeps the last call's contents (nothing in it needs to
  * start at zero); calls that overlap on the GPU, on any streams, race.

@@ -292,12 +292,12 @@ def decode_step_noalloc(p: Plan, query, kv_cache, num_cache_blocks: int, block_t
     B, Hk, QG, D = p.num_seqs, p.num_kv_heads, p.query_group_size, p.head_dim
     out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     args = (
-        _need(query, "query", (torch.bfloat16, torch.int16, torch.uint16), B * Hk * QG * D * 2),
+        _need(query, "query", (torch.bfloat16, torch.int16, torch.uint16), B * Hk * QG * D * 2, host_ok=True),
         _need(kv_cache, "kv_cache", None, num_cache_blocks * p.cache_block_bytes),
         ctypes.c_longlong(num_cache_blocks),
-        _need(block_table, "block_table", torch.int32, B * p.max_blocks_per_seq * 4),
-        _need(context_lens, "context_lens", torch.int32, B * 4),
-        _need(out, "out", (torch.float32, torch.bfloat16), B * Hk * QG * D * out.element_size()),
+        _need(block_table, "block_table", torch.int32, B * p.max_blocks_per_seq * 4, host_ok=True),
+        _need(context_lens, "context_lens", torch.int32, B * 4, host_ok=True),
+        _need(out, "out", (torch.float32, torch.bfloat16), B * Hk * QG * D * out.element_size(), host_ok=True),
         ctypes.c_int(out_dtype),
         None if err_word is None else _need(err_word, "err_word", torch.int32, 4),
         _stream(stream),

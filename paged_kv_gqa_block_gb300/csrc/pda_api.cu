@@ -42,15 +42,18 @@ __global__ void __launch_bounds__(kReduceRows * 32) pda_reduce_kernel(const Redu
     const int q = (blockIdx.x - unit * groups) * kReduceRows + (threadIdx.x >> 5);
     const int b = unit / r.Hk, h = unit - b * r.Hk;
     const int lane = threadIdx.x & 31, d4 = lane << 2;
-    int ctx = __ldg(r.context_lens + b);   // written before the partition pass: no need to wait
+    // Everything this kernel reads, the context lengths included, is read after the wait: a kernel
+    // that ran before the partition pass (an append, or an in-place ctx += 1) may still be in
+    // flight when this grid is scheduled, and only the wait orders its writes before these reads.
+    grid_dependency_wait();
+    if (q >= r.QG) return;
+    int ctx = r.context_lens[b];
     if (ctx < 0 || ctx > r.MB * r.BS) {
         if (h == 0 && q == 0 && lane == 0 && r.err_word) atomicOr(r.err_word, PDA_ERRW_BAD_CONTEXT_LEN);
         ctx = 0;
     }
     const int nv = (ctx + r.W - 1) / r.W;
     const long long base = (long long)unit * r.P * r.QG + q;   // index of (unit, p = 0, q)
-    grid_dependency_wait();
-    if (q >= r.QG) return;
 
     const float* op = r.partial_out + base * kHeadDim + d4;
     const int pstride = r.QG * kHeadDim;

@@ -371,7 +371,9 @@ struct Decode {
         fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 16));
         if (!(fv > 0.f)) fv = 1.f;
         const float rF = rcp_approx(fv);   // acc and F move together: only their product matters
-        const float ratio = F * rF;        // acc holds true_acc / F: rebase it on this step's factor
+        // acc holds true_acc / F: rebase it on this step's factor (exactly 1 when F is unchanged,
+        // which F * rcp(F) need not be)
+        const float ratio = fv == F ? 1.f : F * rF;
         F = fv;
 #pragma unroll
         for (int tl = 0; tl < NTL; ++tl) {
@@ -467,7 +469,7 @@ struct Decode {
                 fv = fmaxf(fv, __shfl_xor_sync(kFull, fv, 16));
                 if (!(fv > 0.f)) fv = 1.f;
                 const float r = rcp_approx(fv);
-                ratio = F * r;   // acc holds true_acc / F: rebase it on the new factor
+                ratio = fv == F ? 1.f : F * r;   // acc holds true_acc / F: rebase it on the new factor
                 F = fv;
                 rF = r;
             }

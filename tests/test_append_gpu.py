@@ -86,3 +86,35 @@ def test_append_data_errors(pda):
     torch.cuda.synchronize()
     assert int(err.item()) & pda.ERRW_BAD_POSITION and int(err.item()) & pda.ERRW_BAD_BLOCK_ID
     assert torch.equal(before, d["cache"])
+
+
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
+def test_in_stream_context_update_is_ordered_before_decode_and_reduce(oracle_mod, pda, kv):
+    # A serving loop on one stream: append the new token at position ctx, add 1 to the device
+    # context lengths in place, then the partition pass and the reduce, with no host sync in
+    # between.  Both kernels must see the lengths the in-place update wrote (the reduce reads them
+    # only after its grid-dependency wait).  Three steps in a row, each against the oracle.
+    ctx0 = (255, 256, 511, 17)
+    w = wl.small(num_seqs=len(ctx0), num_kv_heads=2, query_group_size=8, kv_block_size=16, ctx=ctx0, kv_dtype=kv,
+                 seed=73, max_blocks_per_seq=40)
+    inp = wl.generate(w)
+    d = to_device(inp)
+    p = plan_for(w)
+    rng = np.random.default_rng(5)
+    cache = inp.cache.copy()
+    ctx = inp.context_lens.copy()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for step in range(3):
+        k, v = new_tokens(w, rng)
+        pda.append_kv(p, torch.from_numpy(k.view(np.int16)).cuda(), torch.from_numpy(v.view(np.int16)).cuda(),
+                      d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"], err_word=err)
+        d["context_lens"].add_(1)
+        out = pda.decode_step(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"],
+                              out_dtype=torch.float32, err_word=err)
+        got = out.cpu().numpy()          # the one host synchronisation of the step
+        cache = oracle.append_kv(oh.problem(w), cache, k, v, inp.block_table, ctx)
+        ctx = ctx + 1
+        ref = oh.run_oracle(wl.Inputs(w, inp.query, cache, inp.block_table, ctx))["out"]
+        assert int(err.item()) == 0
+        tol = 2e-3 if kv == wl.KV_BF16 else 1e-2
+        assert np.abs(got - ref).max() <= tol, f"step {step}"

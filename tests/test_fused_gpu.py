@@ -103,3 +103,27 @@ def test_fused_full_size_equals_two_launch(pda, name):
     inp = wl.generate(wl.WORKLOADS[name])
     two, fused = run_both(pda, inp, repeats=1)
     assert np.array_equal(fused[0], two)
+
+
+@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
+def test_fused_repeat_runs_are_bitwise_identical(pda, kv):
+    # the fused step's merge runs in whichever warp arrives last, but always in partition order
+    w = wl.small(num_seqs=4, num_kv_heads=2, ctx=(1000, 3, 513, 2000), seed=36, kv_dtype=kv)
+    inp = wl.generate(w)
+    d = to_device(inp)
+    p = plan_for(w)
+    ws = pda.workspace(p, "cuda")
+    cnt = pda.counters(p, "cuda")
+    outs, parts = [], []
+    for _ in range(3):
+        o = torch.empty((w.num_seqs, w.num_q_heads, 128), dtype=torch.float32, device="cuda")
+        pda.decode_fused(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"],
+                         ws["partial_out"], ws["exp_sums"], ws["max_logits"], cnt, o)
+        torch.cuda.synchronize()
+        outs.append(o.cpu().numpy())
+        parts.append([ws[k].cpu().numpy().copy() for k in ("partial_out", "exp_sums", "max_logits")])
+    for o, pr in zip(outs[1:], parts[1:]):
+        assert np.array_equal(o.view(np.int32), outs[0].view(np.int32))
+        # the partials of multi-partition units (single-partition units write the output directly)
+        for a, b in zip(pr, parts[0]):
+            assert np.array_equal(a.view(np.int32), b.view(np.int32))
