@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--variant", type=int, default=0, choices=[0, 1, 2],
+                    help="partition-kernel layout for --workload: 0 automatic, 1 head warps, 2 head groups (fp8)")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="time only --workload (by default the other configurations are timed too)")
     return ap.parse_args()
@@ -273,11 +275,12 @@ def run_reference(args, rank, world):
 class _Step:
     """One workload resident on the device: inputs, plan, workspace, and the calls of one step."""
 
-    def __init__(self, pda, w, inp, dev, stream, path):
+    def __init__(self, pda, w, inp, dev, stream, path, variant=0):
         import torch
         self.w, self.inp, self.path, self.stream, self.pda = w, inp, path, stream, pda
         self.p = pda.plan(w.num_seqs, w.num_kv_heads, w.query_group_size, w.kv_block_size, w.max_blocks_per_seq,
-                          w.tile_groups_per_partition, w.max_partitions, w.kv_dtype, w.softmax_scale)
+                          w.tile_groups_per_partition, w.max_partitions, w.kv_dtype, w.softmax_scale,
+                          kernel_variant=variant)
         # the step's per-call inputs (query, block table, context lengths) live in one device buffer,
         # so that the end-to-end loop moves them from host memory with a single copy
         parts = [inp.query.view(np.uint8).reshape(-1), inp.block_table.view(np.uint8).reshape(-1),
@@ -394,7 +397,7 @@ def run_ours(args, rank, world, local_rank):
     if args.graph:      # graphs are captured on a non-default stream: run everything on one
         torch.cuda.set_stream(torch.cuda.Stream(dev))
     stream = torch.cuda.current_stream(dev)
-    S = _Step(pda, w, inp, dev, stream, args.path)
+    S = _Step(pda, w, inp, dev, stream, args.path, args.variant)
     step = S.step
 
     for _ in range(args.warmup):
@@ -533,6 +536,7 @@ def run_ours(args, rank, world, local_rank):
                             "d2h_bytes_per_step": int(w.num_seqs * w.num_q_heads * w.head_dim * 2),
                             "how": "one copy of the packed inputs in, one copy of the output out"},
         "gpu_launches": (1 if args.path == "fused" else 2) * args.steps,
+        "kernel_variant": args.variant,
         "step_path": ("pda_decode_fused (one launch)" if args.path == "fused" else "pda_decode + pda_reduce") +
                      (", replayed from a CUDA graph" if args.graph else ""),
         "decode_launches_timed_separately": dec_steps,

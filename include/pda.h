@@ -18,8 +18,14 @@
  *
  * Conventions for every call
  *   - Pointers named "device" are device pointers owned by the caller; the library allocates
- *     nothing, frees nothing and keeps no per-call state.  The only process-wide state is a
- *     cache of the driver's tensor-map encoder and of per-device occupancy figures.
+ *     nothing, frees nothing and keeps no per-call state.  Process-wide state: a cache of the
+ *     driver's tensor-map encoder and of per-device occupancy figures, and, in every GPU that
+ *     loads the library, two small static arrays: 256 pairs of unit counters used by the fp8
+ *     head-group kernel (each launch takes the next pair; the launch's last CTA returns it to
+ *     zero, so a captured launch can be replayed; fewer than 256 such launches may be in flight
+ *     at once on a device), and the 64 MiB array of pda_decode_step_noalloc.  The first launch
+ *     of the head-group kernel on a device looks up its counters' address; make it before any
+ *     stream capture, and make no launch on a device after cudaDeviceReset in the same process.
  *   - Launches are asynchronous on the caller's stream (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream).  Calls that share output or workspace buffers race
  *     if they overlap on the GPU.
@@ -54,6 +60,7 @@ typedef enum pda_status {
 
 enum { PDA_KV_BF16 = 0, PDA_KV_FP8_E4M3 = 1, PDA_KV_TQ4 = 2 };
 enum { PDA_OUT_BF16 = 0, PDA_OUT_F32 = 1 };
+enum { PDA_VARIANT_AUTO = 0, PDA_VARIANT_HEAD_WARPS = 1, PDA_VARIANT_HEAD_GROUPS = 2 };
 
 /* Bits of the device error word. */
 enum {
@@ -87,6 +94,16 @@ typedef struct pda_plan_t {
                                       always waited for (up to 1 s) before a warp leaves.  No
                                       counterpart on the pages; small values exist for testing
                                       the timeout path.                                          */
+    int kernel_variant;            /* how pda_decode lays out the partition pass on the GPU (the
+                                      results agree within the parity tolerances; each variant is
+                                      deterministic on its own):
+                                        PDA_VARIANT_AUTO (0): chosen at launch from the shape,
+                                        PDA_VARIANT_HEAD_WARPS (1): one warp per (sequence, KV head,
+                                          partition) unit, any format,
+                                        PDA_VARIANT_HEAD_GROUPS (2): one CTA per (sequence, group of
+                                          up to 8 KV heads, partition) unit, fp8 e4m3 only.
+                                      pda_decode_fused always uses head warps.  No counterpart on
+                                      the pages.                                                  */
     /* ---- outputs of pda_plan ---- */
     int num_partitions;            /* P = ceil(MB*BS / W)                                          */
     int partition_tokens;          /* W = G * 256                                                 */

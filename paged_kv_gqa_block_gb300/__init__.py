@@ -32,6 +32,9 @@ ERRW_BAD_BLOCK_ID = 2
 ERRW_PIPELINE_TIMEOUT = 4
 ERRW_BAD_POSITION = 8
 HEAD_DIM = 128
+VARIANT_AUTO = 0
+VARIANT_HEAD_WARPS = 1
+VARIANT_HEAD_GROUPS = 2
 
 STATUS = {0: "PDA_OK", -1: "PDA_ERR_INVALID_ARG", -2: "PDA_ERR_UNSUPPORTED", -3: "PDA_ERR_WORKSPACE_TOO_SMALL",
           -4: "PDA_ERR_LAUNCH", -5: "PDA_ERR_NOT_IMPLEMENTED", -6: "PDA_ERR_CUDA"}
@@ -49,7 +52,7 @@ class Plan(ctypes.Structure):
         ("num_seqs", ctypes.c_int), ("num_kv_heads", ctypes.c_int), ("query_group_size", ctypes.c_int),
         ("head_dim", ctypes.c_int), ("kv_block_size", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
         ("tile_groups_per_partition", ctypes.c_int), ("max_partitions", ctypes.c_int), ("kv_dtype", ctypes.c_int),
-        ("softmax_scale", ctypes.c_float), ("wait_timeout_ns", ctypes.c_int),
+        ("softmax_scale", ctypes.c_float), ("wait_timeout_ns", ctypes.c_int), ("kernel_variant", ctypes.c_int),
         ("num_partitions", ctypes.c_int), ("partition_tokens", ctypes.c_int), ("resolved_tile_groups", ctypes.c_int),
         ("resolved_softmax_scale", ctypes.c_float),
         ("cache_block_bytes", ctypes.c_longlong), ("meta_offset_bytes", ctypes.c_longlong),
@@ -108,9 +111,10 @@ def status_string(status: int) -> str:
 
 def plan(num_seqs: int, num_kv_heads: int, query_group_size: int, kv_block_size: int, max_blocks_per_seq: int,
          tile_groups_per_partition: int = 1, max_partitions: int = 0, kv_dtype: int = KV_BF16,
-         softmax_scale: float = 0.0, head_dim: int = HEAD_DIM, wait_timeout_ns: int = 0) -> Plan:
+         softmax_scale: float = 0.0, head_dim: int = HEAD_DIM, wait_timeout_ns: int = 0,
+         kernel_variant: int = 0) -> Plan:
     p = Plan(num_seqs, num_kv_heads, query_group_size, head_dim, kv_block_size, max_blocks_per_seq,
-             tile_groups_per_partition, max_partitions, kv_dtype, softmax_scale, wait_timeout_ns)
+             tile_groups_per_partition, max_partitions, kv_dtype, softmax_scale, wait_timeout_ns, kernel_variant)
     rc = lib().pda_plan(ctypes.byref(p))
     if rc != 0:
         raise PdaError(rc, "pda_plan")

@@ -188,18 +188,20 @@ static long long token_head_bytes(int kv_dtype) {
     return kv_dtype == PDA_KV_BF16 ? 4ll * kHeadDim : kv_dtype == PDA_KV_FP8_E4M3 ? 2ll * kHeadDim : (long long)kHeadDim;
 }
 
-// K|V bytes of one 16-token tile of one KV head.  Dimensions (innermost first):
+// K|V bytes of one 16-token tile of one KV head (or of heads_per_box consecutive heads).
+// Dimensions (innermost first):
 //   {128 bytes of a chunk, BS slots, chunks per token-head, Hk heads, NB blocks}
 // with strides {-, Hk*token_head_bytes, 128, token_head_bytes, cache_block_bytes}.  The box
-// {128, 16, chunks, 1, 1} lands as [chunk][token][128 B] in shared memory, 128-byte swizzle.
-static bool encode_kv_map(CUtensorMap* m, const void* cache, const pda_plan_t* p, long long nb) {
+// {128, 16, chunks, heads_per_box, 1} lands as [head][chunk][token][128 B] in shared memory,
+// 128-byte swizzle.
+static bool encode_kv_map(CUtensorMap* m, const void* cache, const pda_plan_t* p, long long nb, int heads_per_box = 1) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t thb = (cuuint64_t)token_head_bytes(p->kv_dtype);
     const cuuint32_t chunks = (cuuint32_t)(thb / 128);
     cuuint64_t dims[5] = {128, (cuuint64_t)p->kv_block_size, chunks, (cuuint64_t)p->num_kv_heads, (cuuint64_t)nb};
     cuuint64_t strides[4] = {(cuuint64_t)p->num_kv_heads * thb, 128, thb, (cuuint64_t)p->cache_block_bytes};
-    cuuint32_t box[5] = {128, (cuuint32_t)kTileTokens, chunks, 1, 1};
+    cuuint32_t box[5] = {128, (cuuint32_t)kTileTokens, chunks, (cuuint32_t)heads_per_box, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     // L2 fetches are widened to 256 bytes, or to 128 for TQ4 whose token-head rows are 128 bytes
     // (256 would also bring the next head's row, which another warp may read much later)
@@ -210,9 +212,10 @@ static bool encode_kv_map(CUtensorMap* m, const void* cache, const pda_plan_t* p
 }
 
 // Metadata of one 16-token tile: {BS slots, F fields, Hk heads, NB blocks} starting at the metadata
-// region; box {16, F, 1, 1} lands as [field][token].  fp8: F = 2 fp32 fields (K scale, V scale);
+// region; box {16, F, heads_per_box, 1} lands as [head][field][token].  fp8: F = 2 fp32 fields (K scale, V scale);
 // TQ4: F = 3 fp16 fields (k_norm, v_scale, v_zero).
-static bool encode_scale_map(CUtensorMap* m, const void* cache, const pda_plan_t* p, long long nb) {
+static bool encode_scale_map(CUtensorMap* m, const void* cache, const pda_plan_t* p, long long nb,
+                             int heads_per_box = 1) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const bool tq = p->kv_dtype == PDA_KV_TQ4;
@@ -221,7 +224,7 @@ static bool encode_scale_map(CUtensorMap* m, const void* cache, const pda_plan_t
     cuuint64_t dims[4] = {(cuuint64_t)p->kv_block_size, fields, (cuuint64_t)p->num_kv_heads, (cuuint64_t)nb};
     cuuint64_t strides[3] = {(cuuint64_t)p->kv_block_size * esz, (cuuint64_t)p->kv_block_size * esz * fields,
                              (cuuint64_t)p->cache_block_bytes};
-    cuuint32_t box[4] = {(cuuint32_t)kTileTokens, (cuuint32_t)fields, 1, 1};
+    cuuint32_t box[4] = {(cuuint32_t)kTileTokens, (cuuint32_t)fields, (cuuint32_t)heads_per_box, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(m, tq ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<char*>(base),
               dims, strides, box, estr,
@@ -233,7 +236,8 @@ static bool encode_scale_map(CUtensorMap* m, const void* cache, const pda_plan_t
 static int compute_plan(const pda_plan_t* in, pda_plan_t* out) {
     *out = *in;
     if (in->num_seqs < 0 || in->num_kv_heads < 1 || in->max_blocks_per_seq < 1 || in->tile_groups_per_partition < 0 ||
-        in->max_partitions < 0 || in->wait_timeout_ns < 0)
+        in->max_partitions < 0 || in->wait_timeout_ns < 0 || in->kernel_variant < PDA_VARIANT_AUTO ||
+        in->kernel_variant > PDA_VARIANT_HEAD_GROUPS)
         return PDA_ERR_INVALID_ARG;
     if (in->query_group_size != 6 && in->query_group_size != 8 && in->query_group_size != 16)
         return PDA_ERR_UNSUPPORTED;
@@ -241,6 +245,7 @@ static int compute_plan(const pda_plan_t* in, pda_plan_t* out) {
     if (in->head_dim != kHeadDim) return PDA_ERR_UNSUPPORTED;
     if (in->kv_dtype != PDA_KV_BF16 && in->kv_dtype != PDA_KV_FP8_E4M3 && in->kv_dtype != PDA_KV_TQ4)
         return PDA_ERR_UNSUPPORTED;
+    if (in->kernel_variant == PDA_VARIANT_HEAD_GROUPS && in->kv_dtype != PDA_KV_FP8_E4M3) return PDA_ERR_UNSUPPORTED;
     if (!std::isfinite(in->softmax_scale)) return PDA_ERR_INVALID_ARG;
     const long long max_ctx = (long long)in->max_blocks_per_seq * in->kv_block_size;
     if (max_ctx > (1ll << 30)) return PDA_ERR_INVALID_ARG;   // context lengths are int32
@@ -299,6 +304,17 @@ int pda_plan(pda_plan_t* plan) {
 }  // extern "C"
 
 namespace pda {
+// Head groups (fp8) when asked for, or, with PDA_VARIANT_AUTO, when the groups hold 4 heads and
+// the plan has room for at least two (sequence, head group, partition) units per resident CTA
+// (two per SM); otherwise head warps.
+static bool use_head_groups(const pda_plan_t* plan) {
+    if (plan->kernel_variant != PDA_VARIANT_AUTO) return plan->kernel_variant == PDA_VARIANT_HEAD_GROUPS;
+    const int HG = group_heads(plan->num_kv_heads);
+    if (HG < 4) return false;
+    const long long units = (long long)plan->num_seqs * (plan->num_kv_heads / HG) * plan->num_partitions;
+    return units >= 2ll * 2 * device_sm_count();
+}
+
 // The partition pass; with `fused`, the same launch also combines each (sequence, KV head)'s
 // partials into `out` (last-arriving partition merges, counters re-armed to zero).
 static int decode_launch(const pda_plan_t* plan, const void* query, const void* kv_cache, long long num_cache_blocks,
@@ -346,9 +362,18 @@ static int decode_launch(const pda_plan_t* plan, const void* query, const void* 
     a.out = out;
     a.out_f32 = out_dtype == PDA_OUT_F32;
 
+    a.HG = 1;
+    a.sched = nullptr;
     CUtensorMap kv_map, sc_map;
-    if (!encode_kv_map(&kv_map, kv_cache, plan, num_cache_blocks)) return PDA_ERR_LAUNCH;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!fused && plan->kv_dtype == PDA_KV_FP8_E4M3 && use_head_groups(plan)) {
+        a.HG = group_heads(plan->num_kv_heads);
+        if (!encode_kv_map(&kv_map, kv_cache, plan, num_cache_blocks, a.HG) ||
+            !encode_scale_map(&sc_map, kv_cache, plan, num_cache_blocks, a.HG))
+            return PDA_ERR_LAUNCH;
+        return launch_decode_fp8_groups(a, kv_map, sc_map, s);
+    }
+    if (!encode_kv_map(&kv_map, kv_cache, plan, num_cache_blocks)) return PDA_ERR_LAUNCH;
     if (plan->kv_dtype == PDA_KV_BF16) return launch_decode_bf16(a, kv_map, fused, s);
     if (!encode_scale_map(&sc_map, kv_cache, plan, num_cache_blocks)) return PDA_ERR_LAUNCH;
     if (tq) return launch_decode_tq4(a, kv_map, sc_map, s);

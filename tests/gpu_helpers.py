@@ -32,10 +32,13 @@ def decode_any(p, w, d, ws, err=None):
                    ws["partial_out"], ws["exp_sums"], ws["max_logits"], err_word=err)
 
 
-def plan_for(w: wl.Workload, G=None):
+def plan_for(w: wl.Workload, G=None, variant=0):
+    """The plan of a workload; `variant` selects the partition kernel's layout (0 = automatic,
+    1 = head warps, 2 = head groups, fp8 only)."""
     import paged_kv_gqa_block_gb300 as pda
     return pda.plan(w.num_seqs, w.num_kv_heads, w.query_group_size, w.kv_block_size, w.max_blocks_per_seq,
-                    w.tile_groups_per_partition if G is None else G, w.max_partitions, w.kv_dtype, w.softmax_scale)
+                    w.tile_groups_per_partition if G is None else G, w.max_partitions, w.kv_dtype, w.softmax_scale,
+                    kernel_variant=variant)
 
 
 def sentinel_ws(p, dev="cuda"):
@@ -45,11 +48,11 @@ def sentinel_ws(p, dev="cuda"):
     return {"partial_out": mk(so), "exp_sums": mk(ss), "max_logits": mk(ss)}
 
 
-def run_gpu(inp: wl.Inputs, G=None, dev="cuda", d=None):
+def run_gpu(inp: wl.Inputs, G=None, dev="cuda", d=None, variant=0):
     """Partition pass + reduce (fp32 and bf16 outputs).  Returns numpy arrays and the error word."""
     import paged_kv_gqa_block_gb300 as pda
     w = inp.workload
-    p = plan_for(w, G)
+    p = plan_for(w, G, variant)
     d = d or to_device(inp, dev)
     ws = sentinel_ws(p, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -78,3 +81,8 @@ def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
     """Half a bf16 ulp at |x| (8 significant bits)."""
     ax = np.maximum(np.abs(x), 2.0 ** -126)
     return 2.0 ** (np.floor(np.log2(ax)) - 8)
+
+
+# (KV format, partition-kernel variant) pairs that cover every kernel: fp8 runs on head warps and
+# on head groups; bf16 and TQ4 have head warps only
+KV_VARIANTS = [(wl.KV_BF16, 0), (wl.KV_FP8_E4M3, 1), (wl.KV_FP8_E4M3, 2), (wl.KV_TQ4, 0)]

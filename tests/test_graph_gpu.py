@@ -7,7 +7,7 @@ import torch
 
 from paged_kv_gqa_block_gb300 import workloads as wl
 from tests import oracle_helpers as oh
-from tests.gpu_helpers import plan_for, to_device
+from tests.gpu_helpers import KV_VARIANTS, plan_for, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -20,13 +20,13 @@ def pda():
     return pda
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
-def test_captured_step_replays_and_follows_context_lengths(oracle_mod, pda, kv):
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
+def test_captured_step_replays_and_follows_context_lengths(oracle_mod, pda, kv, variant):
     ctx = (700, 33, 256, 1500)
-    w = wl.small(num_seqs=4, num_kv_heads=2, ctx=ctx, kv_dtype=kv, seed=80, max_blocks_per_seq=100)
+    w = wl.small(num_seqs=4, num_kv_heads=4, ctx=ctx, kv_dtype=kv, seed=80, max_blocks_per_seq=100)
     inp = wl.generate(w)
     d = to_device(inp)
-    p = plan_for(w)
+    p = plan_for(w, variant=variant)
     ws = pda.workspace(p, "cuda")
     out = torch.empty((w.num_seqs, w.num_q_heads, 128), dtype=torch.float32, device="cuda")
     s = torch.cuda.Stream()

@@ -20,7 +20,7 @@ import torch
 
 from paged_kv_gqa_block_gb300 import workloads as wl
 from tests import oracle_helpers as oh
-from tests.gpu_helpers import bf16_half_ulp, is_sentinel, run_gpu, to_device
+from tests.gpu_helpers import KV_VARIANTS, bf16_half_ulp, is_sentinel, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -82,7 +82,7 @@ def check_against_oracle(inp, res, ref, units=None):
 
 
 SWEEP = [
-    # (kv dtype, QG, BS, G, Hk, context lengths)
+    # (kv dtype, QG, BS, G, Hk, context lengths); fp8 shapes run on both fp8 kernels
     (wl.KV_BF16, 8, 16, 1, 2, (1, 15, 16, 17, 255, 256, 257, 700)),
     (wl.KV_BF16, 6, 32, 1, 3, (2, 31, 33, 513, 1000)),
     (wl.KV_BF16, 16, 16, 2, 2, (1, 511, 512, 513, 1600)),
@@ -98,18 +98,30 @@ SWEEP = [
 ]
 
 
-@pytest.mark.parametrize("kv,QG,BS,G,Hk,ctx", SWEEP)
-def test_sweep_matches_oracle(oracle_mod, kv, QG, BS, G, Hk, ctx):
+SWEEP += [
+    # head groups of 8 (one group, and four), 4, 6 and 5 heads
+    (wl.KV_FP8_E4M3, 6, 16, 1, 8, (1, 17, 255, 256, 257, 1100, 4000)),
+    (wl.KV_FP8_E4M3, 8, 32, 5, 8, (1279, 1281, 40, 6000)),
+    (wl.KV_FP8_E4M3, 6, 16, 1, 32, (700, 33)),
+    (wl.KV_FP8_E4M3, 16, 16, 2, 4, (513, 2000, 1)),
+    (wl.KV_FP8_E4M3, 8, 32, 1, 12, (300, 901)),
+    (wl.KV_FP8_E4M3, 6, 16, 1, 5, (64, 777)),
+]
+SWEEP_CASES = [(*c, v) for c in SWEEP for v in ((1, 2) if c[0] == wl.KV_FP8_E4M3 else (0,))]
+
+
+@pytest.mark.parametrize("kv,QG,BS,G,Hk,ctx,variant", SWEEP_CASES)
+def test_sweep_matches_oracle(oracle_mod, kv, QG, BS, G, Hk, ctx, variant):
     w = wl.small(num_seqs=len(ctx), num_kv_heads=Hk, query_group_size=QG, kv_block_size=BS, ctx=ctx, kv_dtype=kv,
-                 tile_groups_per_partition=G, seed=100 + QG + BS + G, extra_blocks=5)
+                 tile_groups_per_partition=G, seed=100 + QG + BS + G + Hk, extra_blocks=5)
     inp = wl.generate(w)
-    res = run_gpu(inp)
+    res = run_gpu(inp, variant=variant)
     ref = oh.run_oracle(inp, partials=True, G=G)
     check_against_oracle(inp, res, ref)
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
-def test_more_units_than_warps(oracle_mod, kv):
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
+def test_more_units_than_warps(oracle_mod, kv, variant):
     # 2600 to 3000 (sequence, KV head, partition) units: more than the persistent grid has warps,
     # so warps take tile-balanced runs of several units (fewer units give one unit per warp)
     rng = np.random.default_rng(9)
@@ -117,11 +129,11 @@ def test_more_units_than_warps(oracle_mod, kv):
     w = wl.small(num_seqs=120, num_kv_heads=8, query_group_size=6, kv_block_size=16, ctx=ctx, kv_dtype=kv, seed=41)
     inp = wl.generate(w)
     assert sum(8 * -(-c // 256) for c in ctx) > 2432
-    check_against_oracle(inp, run_gpu(inp), oh.run_oracle(inp, partials=True))
+    check_against_oracle(inp, run_gpu(inp, variant=variant), oh.run_oracle(inp, partials=True))
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
-def test_large_batch_of_short_contexts(oracle_mod, kv):
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
+def test_large_batch_of_short_contexts(oracle_mod, kv, variant):
     # 1500 sequences: every lane of the work scan walks 47 of them; contexts 0-300 tokens (one or
     # two partitions, some empty), sampled units checked against the oracle with their partials
     rng = np.random.default_rng(13)
@@ -129,28 +141,28 @@ def test_large_batch_of_short_contexts(oracle_mod, kv):
     w = wl.small(num_seqs=1500, num_kv_heads=2, query_group_size=8, kv_block_size=16, ctx=ctx, kv_dtype=kv, seed=43,
                  max_blocks_per_seq=19)
     inp = wl.generate(w)
-    res = run_gpu(inp)
+    res = run_gpu(inp, variant=variant)
     units = np.sort(rng.choice(1500 * 2, size=200, replace=False))
     check_against_oracle(inp, res, oh.run_oracle(inp, partials=True, units=units), units=units)
     empty = [b for b, c in enumerate(ctx) if c == 0]
     assert empty and np.all(res["out"][empty] == 0)
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
-def test_many_kv_heads(oracle_mod, kv):
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
+def test_many_kv_heads(oracle_mod, kv, variant):
     # 32 KV heads of QG 6 (192 query heads): the head dimension of the tensor maps and the
     # per-head metadata offsets at a large head count; 1056 units (tile-balanced on the 912-warp
     # bf16 grid, one unit per warp on the 1824-warp fp8 and TQ4 grids)
     ctx = (4000, 1, 1300, 700, 256, 1500)
     w = wl.small(num_seqs=6, num_kv_heads=32, query_group_size=6, kv_block_size=16, ctx=ctx, kv_dtype=kv, seed=44)
     inp = wl.generate(w)
-    res = run_gpu(inp)
+    res = run_gpu(inp, variant=variant)
     units = np.sort(np.random.default_rng(3).choice(6 * 32, size=48, replace=False))
     check_against_oracle(inp, res, oh.run_oracle(inp, partials=True, units=units), units=units)
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
-def test_one_unit_per_warp(oracle_mod, kv):
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
+def test_one_unit_per_warp(oracle_mod, kv, variant):
     # room for 16 x 8 x 16 = 2048 partitions (more than the grid's warps) but short contexts
     # give at most 16 x 8 x 3 = 384 non-empty ones: each warp takes one whole unit
     rng = np.random.default_rng(11)
@@ -158,29 +170,29 @@ def test_one_unit_per_warp(oracle_mod, kv):
     w = wl.small(num_seqs=16, num_kv_heads=8, query_group_size=8, kv_block_size=16, ctx=ctx, kv_dtype=kv, seed=42,
                  max_blocks_per_seq=256)
     inp = wl.generate(w)
-    res = run_gpu(inp)
+    res = run_gpu(inp, variant=variant)
     assert res["plan"].num_partitions == 16
     check_against_oracle(inp, res, oh.run_oracle(inp, partials=True))
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
-def test_more_than_64_partitions_and_empty_sequences(oracle_mod, kv):
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
+def test_more_than_64_partitions_and_empty_sequences(oracle_mod, kv, variant):
     # the longest sequence has 79 partitions of 256 tokens: the reduce holds (m_p, l_p) of 64
     # partitions per row in registers and reloads the rest; empty sequences sit in between
     ctx = (20000, 0, 16385, 300, 0, 1)
     w = wl.small(num_seqs=6, num_kv_heads=2, query_group_size=8, kv_block_size=32, ctx=ctx, kv_dtype=kv, seed=71)
     inp = wl.generate(w)
-    res = run_gpu(inp)
+    res = run_gpu(inp, variant=variant)
     assert res["plan"].num_partitions == 79
     check_against_oracle(inp, res, oh.run_oracle(inp, partials=True))
     assert np.all(res["out"][[1, 4]] == 0) and np.all(res["out_bf16"][[1, 4]] == 0)
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
-def test_every_context_empty(oracle_mod, kv):
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
+def test_every_context_empty(oracle_mod, kv, variant):
     w = wl.small(num_seqs=3, num_kv_heads=2, ctx=(0, 0, 0), kv_dtype=kv, seed=72, max_blocks_per_seq=4)
     inp = wl.generate(w)
-    res = run_gpu(inp)
+    res = run_gpu(inp, variant=variant)
     assert res["err"] == 0
     assert np.all(res["out"] == 0) and np.all(res["out_bf16"] == 0)
     for key in ("part_o", "part_m", "part_l"):
@@ -194,8 +206,8 @@ def test_key_bias_workload_small(oracle_mod):
     check_against_oracle(inp, run_gpu(inp), oh.run_oracle(inp, partials=True))
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
-def test_zero_keys_count_probe_is_exact(oracle_mod, kv):
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
+def test_zero_keys_count_probe_is_exact(oracle_mod, kv, variant):
     ctx = (600, 256, 1)
     w = wl.small(num_seqs=3, num_kv_heads=2, ctx=ctx, kv_dtype=kv, seed=31)
     rng = np.random.default_rng(0)
@@ -203,7 +215,7 @@ def test_zero_keys_count_probe_is_exact(oracle_mod, kv):
     V = [rng.standard_normal((c, 2, 128)).astype(np.float32) for c in ctx]
     q = rng.standard_normal((3, w.num_q_heads, 128)).astype(np.float32)
     inp = oh.build_from_values(w, q, K, V, wl.draw_block_table(w, rng))
-    res = run_gpu(inp)
+    res = run_gpu(inp, variant=variant)
     assert res["err"] == 0
     for b, c in enumerate(ctx):
         nv = -(-c // 256)
@@ -225,10 +237,10 @@ def stored_v_rows_f32(w, V):
     return oh.stored_values(w, V).astype(np.float32).astype(np.float64)
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
 @pytest.mark.parametrize("BS,ctx,js", [(16, 37, (0, 15, 16, 36)), (16, 700, (0, 255, 256, 511, 699)),
                                        (32, 700, (31, 32, 300, 699))])
-def test_one_hot_probe_returns_the_stored_row_exactly(oracle_mod, kv, BS, ctx, js):
+def test_one_hot_probe_returns_the_stored_row_exactly(oracle_mod, kv, variant, BS, ctx, js):
     # One key j points along the query (a logit gap above 140, so every other weight is exactly
     # 0 in fp32 and p_j = 1); the output is then the stored V row j itself, bit for bit, which
     # pins the block-table walk (entry t/BS, slot t%BS) of every format.  Every V row has the same
@@ -248,16 +260,16 @@ def test_one_hot_probe_returns_the_stored_row_exactly(oracle_mod, kv, BS, ctx, j
         vj = stored_v_rows_f32(w, V)[j]
         ref = oh.run_oracle(inp)["out"][0].reshape(2, 8, 128)
         assert np.allclose(ref, vj[:, None, :], rtol=0, atol=1e-6)     # the probe is what it claims
-        res = run_gpu(inp)
+        res = run_gpu(inp, variant=variant)
         assert res["err"] == 0
         out = res["out"][0].reshape(2, 8, 128)
         for h in range(2):
             assert np.array_equal(out[h], np.broadcast_to(vj[h], (8, 128))), f"j={j} h={h}"
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
 @pytest.mark.parametrize("QG", [8, 16])
-def test_running_maximum_and_v_scale_swings(oracle_mod, kv, QG):
+def test_running_maximum_and_v_scale_swings(oracle_mod, kv, variant, QG):
     # Key magnitudes that grow 160-fold across every 256-token partition move the running
     # maximum by several times 2^8 within a partition; the next sequence has them shrink instead
     # (the maximum is set by the first tiles); V rows jump between magnitude 1 and 2^-8 every
@@ -277,25 +289,25 @@ def test_running_maximum_and_v_scale_swings(oracle_mod, kv, QG):
         K.append((rng.standard_normal((c, 2, 128)) * gk[:, None, None]).astype(np.float32))
         V.append((rng.standard_normal((c, 2, 128)) * gv[:, None, None]).astype(np.float32))
     inp = oh.build_from_values(w, q, K, V, wl.draw_block_table(w, rng))
-    res = run_gpu(inp)
+    res = run_gpu(inp, variant=variant)
     assert res["plan"].partition_tokens == 256
     check_against_oracle(inp, res, oh.run_oracle(inp, partials=True))
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
 @pytest.mark.parametrize("BS", [16, 32])
-def test_block_relocation_is_bitwise_invariant(kv, BS):
+def test_block_relocation_is_bitwise_invariant(kv, variant, BS):
     # moving every block of the pool (data and metadata) and rewriting the tables to match changes
     # no bit of the output or of any partial: the arithmetic follows the logical token order only
     w = wl.small(num_seqs=2, num_kv_heads=2, kv_block_size=BS, ctx=(900, 77), seed=33, extra_blocks=11, kv_dtype=kv)
     inp = wl.generate(w)
-    a = run_gpu(inp)
+    a = run_gpu(inp, variant=variant)
     perm = np.random.default_rng(0).permutation(w.num_cache_blocks)
     blocks = inp.cache.reshape(w.num_cache_blocks, w.cache_block_bytes)
     moved = np.empty_like(blocks)
     moved[perm] = blocks
     b = run_gpu(wl.Inputs(w, inp.query, moved.reshape(-1), perm[inp.block_table].astype(np.int32), inp.context_lens,
-                          inp.extra))
+                          inp.extra), variant=variant)
     assert a["err"] == 0 and b["err"] == 0
     assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["out_bf16"], b["out_bf16"])
     for k in ("part_o", "part_m", "part_l"):
@@ -310,13 +322,13 @@ def test_short_contexts_do_not_depend_on_G():
     assert np.array_equal(r1["out"], r2["out"]) and np.array_equal(r1["out"], r5["out"])
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
-def test_repeat_runs_are_bitwise_identical(kv):
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
+def test_repeat_runs_are_bitwise_identical(kv, variant):
     # the work assignment is a function of the inputs only, and every sum has a fixed order
     w = wl.small(num_seqs=4, num_kv_heads=2, ctx=(1000, 3, 513, 2000), seed=35, kv_dtype=kv)
     inp = wl.generate(w)
     d = to_device(inp)
-    a, b = run_gpu(inp, d=d), run_gpu(inp, d=d)
+    a, b = run_gpu(inp, d=d, variant=variant), run_gpu(inp, d=d, variant=variant)
     assert np.array_equal(a["out"], b["out"])
     for k in ("part_o", "part_m", "part_l"):     # compare bits: unwritten slots hold the NaN sentinel
         assert np.array_equal(a[k].view(np.int32), b[k].view(np.int32))
@@ -348,13 +360,44 @@ def test_bad_block_id_sets_error_bit_without_faulting():
 
 
 # ---------------------------------------------------------------- full-size workloads
-@pytest.mark.parametrize("name", wl.WORKLOAD_ORDER)
-def test_full_size_workload_every_unit(oracle_mod, name):
+FULL_CASES = [(n, 0) for n in wl.WORKLOAD_ORDER] + [
+    (n, v) for n in wl.WORKLOAD_ORDER if wl.WORKLOADS[n].kv_dtype == wl.KV_FP8_E4M3 for v in (1, 2)]
+
+
+@pytest.mark.parametrize("name,variant", FULL_CASES)
+def test_full_size_workload_every_unit(oracle_mod, name, variant):
     # every (sequence, KV head) unit of the configuration, with every partition's partials, in
-    # the launch configuration the bench times
+    # the launch configuration the bench times (variant 0), and for fp8 on each kernel
     w = wl.WORKLOADS[name]
     inp = wl.generate(w)
-    res = run_gpu(inp)
+    res = run_gpu(inp, variant=variant)
     assert res["err"] == 0
     assert np.isfinite(res["out"]).all()
     check_against_oracle(inp, res, oh.run_oracle(inp, partials=True))
+
+
+def test_head_group_counters_return_to_zero_across_many_launches(oracle_mod):
+    # The head-group kernel takes units from a counter pair that its last CTA returns to zero; the
+    # library cycles through 256 such pairs.  600 launches in a row (every pair reused twice) must
+    # all give the same bits as the first, which matches the oracle.
+    import paged_kv_gqa_block_gb300 as pda
+    from tests.gpu_helpers import plan_for, sentinel_ws
+    w = wl.small(num_seqs=6, num_kv_heads=8, query_group_size=6, kv_block_size=16,
+                 ctx=(300, 5000, 17, 2048, 1000, 256), kv_dtype=wl.KV_FP8_E4M3, seed=96)
+    inp = wl.generate(w)
+    d = to_device(inp)
+    p = plan_for(w, variant=2)
+    ws = sentinel_ws(p)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for i in range(600):
+        pda.decode(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"],
+                   ws["partial_out"], ws["exp_sums"], ws["max_logits"], err_word=err)
+        if i in (0, 599):
+            o = torch.empty((w.num_seqs, w.num_q_heads, 128), dtype=torch.float32, device="cuda")
+            pda.reduce(p, d["context_lens"], ws["partial_out"], ws["exp_sums"], ws["max_logits"], o, err_word=err)
+            outs.append(o.cpu().numpy())
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(outs[0].view(np.int32), outs[1].view(np.int32))
+    assert np.abs(outs[0] - oh.run_oracle(inp)["out"]).max() <= TOL[wl.KV_FP8_E4M3]

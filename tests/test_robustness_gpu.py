@@ -12,7 +12,7 @@ import torch
 
 from paged_kv_gqa_block_gb300 import workloads as wl
 from tests import oracle_helpers as oh
-from tests.gpu_helpers import SENTINEL_BITS, decode_any, plan_for, run_gpu, to_device
+from tests.gpu_helpers import KV_VARIANTS, SENTINEL_BITS, decode_any, plan_for, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -45,19 +45,19 @@ def _step(pda, p, d, nb, err=None, out_dtype=torch.float32, ws=None):
 # (not TQ4: its warps are bound by their own arithmetic, every 2 KB tile has landed before its
 # wait begins, so even a 1 ns limit is not reached; the timeout path itself does not depend on
 # the cache format)
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
-def test_wait_timeout_sets_the_error_bit_and_the_next_call_is_correct(oracle_mod, pda, kv):
+@pytest.mark.parametrize("kv,variant", [(wl.KV_BF16, 0), (wl.KV_FP8_E4M3, 1), (wl.KV_FP8_E4M3, 2)])
+def test_wait_timeout_sets_the_error_bit_and_the_next_call_is_correct(oracle_mod, pda, kv, variant):
     # a step big enough to load HBM (every copy then takes microseconds), each wait limited to 1 ns
     w = wl.small(num_seqs=16, num_kv_heads=8, ctx=(8192,) * 16, kv_dtype=kv, seed=61, extra_blocks=0)
     inp = wl.generate(w)
     d = to_device(inp)
     p = pda.plan(w.num_seqs, w.num_kv_heads, w.query_group_size, w.kv_block_size, w.max_blocks_per_seq,
-                 kv_dtype=kv, wait_timeout_ns=1)
+                 kv_dtype=kv, wait_timeout_ns=1, kernel_variant=variant)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     _step(pda, p, d, w.num_cache_blocks, err)
     assert int(err.item()) & pda.ERRW_PIPELINE_TIMEOUT
     assert torch.zeros(1, device="cuda").add_(1).item() == 1.0   # the context is usable
-    res = run_gpu(inp, d=d)   # default limit, same inputs: no error bit, and correct
+    res = run_gpu(inp, d=d, variant=variant)   # default limit, same inputs: no error bit, and correct
     assert res["err"] == 0
     units = [0, 37, 127]
     ref = oh.run_oracle(inp, units=units)["out"]
@@ -90,12 +90,12 @@ def test_cache_blocks_past_4_gib(oracle_mod, pda):
     del big
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
-def test_guard_words_around_every_written_buffer_stay_intact(pda, kv):
-    w = wl.small(num_seqs=3, num_kv_heads=2, ctx=(900, 17, 256), kv_dtype=kv, seed=63)
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
+def test_guard_words_around_every_written_buffer_stay_intact(pda, kv, variant):
+    w = wl.small(num_seqs=3, num_kv_heads=8, ctx=(900, 17, 256), kv_dtype=kv, seed=63)
     inp = wl.generate(w)
     d = to_device(inp)
-    p = plan_for(w)
+    p = plan_for(w, variant=variant)
     G = 64   # guard floats before and after each buffer (256 bytes keep the 16-byte alignment)
 
     def guarded(n):
@@ -123,14 +123,14 @@ def test_guard_words_around_every_written_buffer_stay_intact(pda, kv):
     assert torch.equal(d["cache"], torch.from_numpy(inp.cache).to("cuda"))
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3, wl.KV_TQ4])
-def test_inputs_and_output_in_pinned_host_memory(pda, kv):
+@pytest.mark.parametrize("kv,variant", KV_VARIANTS)
+def test_inputs_and_output_in_pinned_host_memory(pda, kv, variant):
     # query, block table and context lengths read by the kernels across the host link, the output
     # written back the same way: the same bits as with every buffer on the device
-    w = wl.small(num_seqs=4, num_kv_heads=2, ctx=(700, 1, 300, 2000), kv_dtype=kv, seed=64)
+    w = wl.small(num_seqs=4, num_kv_heads=8, ctx=(700, 1, 300, 2000), kv_dtype=kv, seed=64)
     inp = wl.generate(w)
     d = to_device(inp)
-    p = plan_for(w)
+    p = plan_for(w, variant=variant)
     ref = _step(pda, p, d, w.num_cache_blocks).cpu()
     h = {"query": d["query"].cpu().pin_memory(), "block_table": d["block_table"].cpu().pin_memory(),
          "context_lens": d["context_lens"].cpu().pin_memory(), "cache": d["cache"], "centroids": d.get("centroids")}
