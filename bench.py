@@ -46,8 +46,9 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
 L2_CLEAN_READ_BYTES = 256 << 20
 # the files that make up the partition kernel (its ncu counters go stale when one changes)
-PARTITION_KERNEL_SOURCES = ("pda_decode.cuh", "pda_ptx.cuh", "pda_launch.cuh", "pda_internal.h",
-                            "pda_decode_bf16.cu", "pda_decode_fp8.cu", "pda_decode_tq4.cu", "pda_api.cu")
+PARTITION_KERNEL_SOURCES = ("pda_decode.cuh", "pda_group.cuh", "pda_merge.cuh", "pda_ptx.cuh", "pda_launch.cuh",
+                            "pda_internal.h", "pda_decode_bf16.cu", "pda_decode_fp8.cu", "pda_decode_tq4.cu",
+                            "pda_api.cu")
 
 
 def parse():

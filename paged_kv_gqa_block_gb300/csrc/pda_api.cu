@@ -11,138 +11,66 @@
 #include "pda.h"
 #include "pda_internal.h"
 #include "pda_ptx.cuh"
+#include "pda_merge.cuh"
 
 namespace pda {
 
+constexpr int kMaxReduceWarps = 16;   // query rows of a unit (QG <= 16)
+
 // ------------------------------------------------------------------------- reduce kernel
-// One CTA per (sequence, KV head, group of up to 8 query rows), one warp per query row q.
-// Lane j holds (m_p, l_p) of partitions p = j, j+32, ...; warp reductions give M = max m_p and
-// sum_p w_p with w_p = l_p * e^(m_p - M); then every lane accumulates four output elements,
-// out = sum_p (w_p / sum w) * o_p over p < ceil(ctx / W), in partition order, sixteen partial
-// loads in flight.  The first sixteen partials are requested together with (m_p, l_p), so a
-// row of up to sixteen partitions costs one round trip to L2.  With one partition
-// w_0 / w_0 == 1 exactly, so the partial is copied bit for bit.  Launched as a programmatic
-// dependent of the partition pass: it waits for that grid before reading the partials.
-constexpr int kReduceRegParts = 2;   // partitions held per lane (up to 64); beyond that (m, l) are reloaded
-constexpr int kReduceRows = 8;       // query rows (warps) per CTA
-constexpr int kReduceBatch = 16;     // partial loads in flight per lane
-
-__device__ __forceinline__ void load_partial_batch(const float* op, int pstride, int p0, int nv,
-                                                   float4 (&o)[kReduceBatch]) {
-    const float4* o4 = reinterpret_cast<const float4*>(op);
-    const int s4 = pstride >> 2;   // float4s between partitions (QG * D / 4)
-#pragma unroll
-    for (int j = 0; j < kReduceBatch; ++j)   // clamped index: every load is in bounds, extras weigh 0
-        o[j] = __ldcg(o4 + (long long)min(p0 + j, nv - 1) * s4);
-}
-
-__global__ void __launch_bounds__(kReduceRows * 32) pda_reduce_kernel(const ReduceArgs r) {
-    const int groups = (r.QG + kReduceRows - 1) / kReduceRows;
-    const int unit = blockIdx.x / groups;
-    const int q = (blockIdx.x - unit * groups) * kReduceRows + (threadIdx.x >> 5);
-    const int b = unit / r.Hk, h = unit - b * r.Hk;
-    const int lane = threadIdx.x & 31, d4 = lane << 2;
+// One CTA per (sequence, KV head) unit, one warp per query row; the unit's partials stream through
+// shared memory by bulk copies (merge_unit_smem, pda_merge.cuh).  Launched as a programmatic
+// dependent of the partition pass: it waits for that grid before reading anything.
+__global__ void __launch_bounds__(kMaxReduceWarps * 32, 1) pda_reduce_kernel(const ReduceArgs r) {
+    extern __shared__ __align__(128) float reduce_smem[];
+    __shared__ __align__(8) uint64_t bars[4];   // full[2], empty[2]
     // Everything this kernel reads, the context lengths included, is read after the wait: a kernel
     // that ran before the partition pass (an append, or an in-place ctx += 1) may still be in
     // flight when this grid is scheduled, and only the wait orders its writes before these reads.
     grid_dependency_wait();
-    if (q >= r.QG) return;
+    const int b = (int)(blockIdx.x / r.Hk), h = (int)(blockIdx.x - (unsigned)b * r.Hk);
     int ctx = r.context_lens[b];
     if (ctx < 0 || ctx > r.MB * r.BS) {
-        if (h == 0 && q == 0 && lane == 0 && r.err_word) atomicOr(r.err_word, PDA_ERRW_BAD_CONTEXT_LEN);
+        if (h == 0 && threadIdx.x == 0 && r.err_word) atomicOr(r.err_word, PDA_ERRW_BAD_CONTEXT_LEN);
         ctx = 0;
     }
-    const int nv = (ctx + r.W - 1) / r.W;
-    const long long base = (long long)unit * r.P * r.QG + q;   // index of (unit, p = 0, q)
-
-    const float* op = r.partial_out + base * kHeadDim + d4;
-    const int pstride = r.QG * kHeadDim;
-    float mr[kReduceRegParts], lr[kReduceRegParts];
-#pragma unroll
-    for (int k = 0; k < kReduceRegParts; ++k) {
-        const int p = lane + 32 * k;
-        mr[k] = -INFINITY;
-        lr[k] = 0.f;
-        if (p < nv) {
-            const long long i = base + (long long)p * r.QG;
-            mr[k] = __ldcg(r.max_logits + i);
-            lr[k] = __ldcg(r.exp_sums + i);
-        }
+    const uint32_t bar0 = smem_addr(bars);
+    if (threadIdx.x == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar0 + 8, 1);
+        mbar_init(bar0 + 16, (uint32_t)r.QG);
+        mbar_init(bar0 + 24, (uint32_t)r.QG);
+        fence_mbar_init();
     }
-    float4 o[kReduceBatch];
-    if (nv > 0) load_partial_batch(op, pstride, 0, nv, o);   // in flight with (m, l)
-    float M = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < kReduceRegParts; ++k) M = fmaxf(M, mr[k]);
-    for (int p = lane + 32 * kReduceRegParts; p < nv; p += 32)
-        M = fmaxf(M, __ldcg(r.max_logits + base + (long long)p * r.QG));
-#pragma unroll
-    for (int o_ = 16; o_ > 0; o_ >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o_));
-    float wsum = 0.f;
-#pragma unroll
-    for (int k = 0; k < kReduceRegParts; ++k) {
-        lr[k] = partition_weight(lr[k], mr[k], M);   // w_p (0 for p >= nv)
-        wsum = __fadd_rn(wsum, lr[k]);
-    }
-    for (int p = lane + 32 * kReduceRegParts; p < nv; p += 32) {
-        const long long i = base + (long long)p * r.QG;
-        wsum = __fadd_rn(wsum, partition_weight(__ldcg(r.exp_sums + i), __ldcg(r.max_logits + i), M));
-    }
-#pragma unroll
-    for (int o_ = 16; o_ > 0; o_ >>= 1) wsum = __fadd_rn(wsum, __shfl_xor_sync(0xFFFFFFFFu, wsum, o_));
-
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = 0; c0 < nv; c0 += 32) {
-        const int k = c0 >> 5;
-        float coef;
-        if (k < kReduceRegParts) {
-            float w = lr[0];
-#pragma unroll
-            for (int kk = 1; kk < kReduceRegParts; ++kk)
-                if (kk == k) w = lr[kk];
-            coef = __fdiv_rn(w, wsum);
-        } else {
-            const int p = c0 + lane;
-            coef = 0.f;
-            if (p < nv) {
-                const long long i = base + (long long)p * r.QG;
-                coef = __fdiv_rn(partition_weight(__ldcg(r.exp_sums + i), __ldcg(r.max_logits + i), M), wsum);
-            }
-        }
-        const int cn = min(32, nv - c0);
-        for (int j0 = 0; j0 < cn; j0 += kReduceBatch) {
-            if (c0 + j0 > 0) load_partial_batch(op, pstride, c0 + j0, nv, o);
-#pragma unroll
-            for (int j = 0; j < kReduceBatch; ++j) {
-                const float cf = __shfl_sync(0xFFFFFFFFu, coef, (j0 + j) & 31);
-                if (j0 + j < cn) {
-                    acc.x = fmaf(cf, o[j].x, acc.x);
-                    acc.y = fmaf(cf, o[j].y, acc.y);
-                    acc.z = fmaf(cf, o[j].z, acc.z);
-                    acc.w = fmaf(cf, o[j].w, acc.w);
-                }
-            }
-        }
-    }
-    const long long orow = (long long)b * r.Hk * r.QG + (long long)h * r.QG + q;
-    if (r.out_f32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(r.out) + orow * kHeadDim + d4) = acc;
-    } else {
-        uint2 v;
-        v.x = pack_bf16(acc.x, acc.y);
-        v.y = pack_bf16(acc.z, acc.w);
-        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(r.out) + orow * kHeadDim + d4) = v;
-    }
+    __syncthreads();
+    const MergeArgs m{r.partial_out, r.exp_sums, r.max_logits, r.out, r.Hk, r.QG, r.P, r.W, r.out_f32};
+    bool timed_out = false;
+    merge_unit_smem(m, b, h, ctx, reduce_smem, bar0, &timed_out);
+    if (timed_out && (threadIdx.x & 31) == 0 && r.err_word) atomicOr(r.err_word, PDA_ERRW_PIPELINE_TIMEOUT);
 }
 
+static int reduce_smem_bytes(int QG) { return 2 * kMergeChunk * QG * kHeadDim * 4; }
+
 int launch_reduce(const ReduceArgs& r, cudaStream_t stream) {
-    const int groups = (r.QG + kReduceRows - 1) / kReduceRows;
-    const long long ctas = (long long)r.B * r.Hk * groups;
-    const int threads = min(r.QG, kReduceRows) * 32;
+    static bool attr_set[64] = {false};   // the shared-memory limit, set once per device
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PDA_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[dev]) {
+            if (cudaFuncSetAttribute(pda_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     reduce_smem_bytes(kMaxReduceWarps)) != cudaSuccess)
+                return PDA_ERR_LAUNCH;
+            attr_set[dev] = true;
+        }
+    }
+    const long long ctas = (long long)r.B * r.Hk;
+    if (ctas > 0x7FFFFFFFll || r.QG > kMaxReduceWarps) return PDA_ERR_INVALID_ARG;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas);
-    cfg.blockDim = dim3(threads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.blockDim = dim3(r.QG * 32);
+    cfg.dynamicSmemBytes = reduce_smem_bytes(r.QG);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -366,12 +294,15 @@ static int decode_launch(const pda_plan_t* plan, const void* query, const void* 
     a.sched = nullptr;
     CUtensorMap kv_map, sc_map;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (!fused && plan->kv_dtype == PDA_KV_FP8_E4M3 && use_head_groups(plan)) {
+    // the fused step runs on head groups when they hold at least two heads (its counters need two
+    // entries per group), else on head warps
+    if (plan->kv_dtype == PDA_KV_FP8_E4M3 && use_head_groups(plan) &&
+        (!fused || group_heads(plan->num_kv_heads) >= 2)) {
         a.HG = group_heads(plan->num_kv_heads);
         if (!encode_kv_map(&kv_map, kv_cache, plan, num_cache_blocks, a.HG) ||
             !encode_scale_map(&sc_map, kv_cache, plan, num_cache_blocks, a.HG))
             return PDA_ERR_LAUNCH;
-        return launch_decode_fp8_groups(a, kv_map, sc_map, s);
+        return launch_decode_fp8_groups(a, kv_map, sc_map, fused, s);
     }
     if (!encode_kv_map(&kv_map, kv_cache, plan, num_cache_blocks)) return PDA_ERR_LAUNCH;
     if (plan->kv_dtype == PDA_KV_BF16) return launch_decode_bf16(a, kv_map, fused, s);

@@ -23,12 +23,14 @@ int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUte
     return launch_partition<PDA_KV_FP8_E4M3, 2, 4, 8, false>(a, kv_map, sc_map, stream);
 }
 
-// Unit counters of the head-group kernel: kSchedSlots pairs {next unit, CTAs done}, every pair zero
-// between launches (a launch's last CTA returns its pair to zero).  Each launch takes the next pair
-// in turn, so launches in flight at the same time (on other streams) use different pairs as long as
-// fewer than kSchedSlots of them overlap.  The array lives in every GPU that loads the library.
-constexpr int kSchedSlots = 256;
-static __device__ unsigned int g_group_sched[2 * kSchedSlots];
+// Counters of the head-group kernel: kSchedSlots slots of kSchedInts counters ({next unit,
+// producers done} for the partition pass; {next unit, -, queue tail, next row, warps done} for the
+// fused step), every slot zero between launches (each launch's last CTA or warp returns its slot
+// to zero).  Each launch takes the next slot in turn, so launches in flight at the same time (on
+// other streams) use different slots as long as fewer than kSchedSlots of them overlap.  The array
+// lives in every GPU that loads the library.
+constexpr int kSchedSlots = 256, kSchedInts = 8;
+static __device__ unsigned int g_group_sched[kSchedInts * kSchedSlots];
 
 // Device address of this launch's pair (the array's address is looked up once per device).
 static unsigned int* group_sched_slot(int* status) {
@@ -52,7 +54,7 @@ static unsigned int* group_sched_slot(int* status) {
         }
     }
     *status = PDA_OK;
-    return base[dev] + 2 * (int)(seq.fetch_add(1) % kSchedSlots);
+    return base[dev] + kSchedInts * (int)(seq.fetch_add(1) % kSchedSlots);
 }
 
 int group_heads(int Hk) {
@@ -63,23 +65,23 @@ int group_heads(int Hk) {
 
 // Persistent grid of head-group CTAs: (SMs x resident CTAs per SM), each CTA one producer warp
 // and a.HG consumer warps.
-template <int NT, int S, int NWARPS, int MINB>
+template <int NT, int S, int NWARPS, int MINB, bool FUSED>
 static int launch_groups(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
                          cudaStream_t stream) {
-    auto kernel = pda_group_kernel<NT, S, NWARPS, MINB>;
+    auto kernel = pda_group_kernel<NT, S, NWARPS, MINB, FUSED>;
     static int occ_cache[64][kGroupMaxHeads + 1] = {};
     static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PDA_ERR_CUDA;
-    const int threads = 32 * (a.HG + 1);
+    const int threads = 32 * (a.HG + (FUSED ? 2 : 1));   // producer, HG consumers (, merger)
     const int smem = group_smem_bytes(a.HG, S);
-    if (a.HG < 1 || a.HG + 1 > NWARPS) return PDA_ERR_INVALID_ARG;
+    if (a.HG < 1 || threads > 32 * NWARPS || (FUSED && a.HG < 2)) return PDA_ERR_INVALID_ARG;
     int occ;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (occ_cache[dev][a.HG] == 0) {
             if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     group_smem_bytes(NWARPS - 1, S)) != cudaSuccess)
+                                     group_smem_bytes(kGroupMaxHeads, S)) != cudaSuccess)
                 return PDA_ERR_LAUNCH;
             int o = 0;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, threads, smem) != cudaSuccess || o < 1)
@@ -112,12 +114,16 @@ static int launch_groups(const DecodeArgs& a, const CUtensorMap& kv_map, const C
 }
 
 int launch_decode_fp8_groups(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
-                             cudaStream_t stream) {
-    // up to 4 heads a CTA: two CTAs of up to 5 warps per SM, each with 6 stages of up to 17 KB (two
-    // independent producers per SM, whose consumers reach their unit boundaries at different times,
-    // measured faster than one CTA of 8 heads with 6 stages of 33 KB)
-    if (a.QG <= 8) return launch_groups<1, 6, 5, 2>(a, kv_map, sc_map, stream);
-    return launch_groups<2, 6, 5, 2>(a, kv_map, sc_map, stream);
+                             bool fused, cudaStream_t stream) {
+    // up to 4 heads a CTA: two CTAs of up to 5 warps (6 for the fused step) per SM, each with 6
+    // stages of up to 17 KB (two independent producers per SM, whose consumers reach their unit
+    // boundaries at different times, measured faster than one CTA of 8 heads with 6 stages of 33 KB)
+    if (fused) {
+        if (a.QG <= 8) return launch_groups<1, 6, 6, 2, true>(a, kv_map, sc_map, stream);
+        return launch_groups<2, 6, 6, 2, true>(a, kv_map, sc_map, stream);
+    }
+    if (a.QG <= 8) return launch_groups<1, 6, 5, 2, false>(a, kv_map, sc_map, stream);
+    return launch_groups<2, 6, 5, 2, false>(a, kv_map, sc_map, stream);
 }
 
 }  // namespace pda

@@ -29,6 +29,7 @@
 #pragma once
 
 #include "pda_decode.cuh"
+#include "pda_merge.cuh"
 
 namespace pda {
 
@@ -51,21 +52,38 @@ struct GroupUnit {
     bool valid;
 };
 
-// The CTA's unit list, derived by one warp from the context lengths.  Lane l looks after
-// sequences [b0, b1); NF and NP count the full-partition and partial-partition units (x NG head
-// groups each).  `above` is the CTA's table of partial sequences per tile-count bucket: above[t] =
-// number of sequences whose partial partition falls in a bucket above t (built once per CTA).
+// The launch's unit order, in three classes:
+//   L: every unit of the long sequences (at least kGroupLongPartitions partitions), in (sequence,
+//      head group, partition) order;
+//   F: the full partitions of the other sequences, in the same order;
+//   P: the partial last partitions of the other sequences, by decreasing tile count (bucket), then
+//      sequence, then head group.
+// Longest first keeps the end of the launch to the smallest units, and the long sequences, whose
+// partials take the longest to combine, are complete well before the end.
+// GroupSched is the order as one warp derives it from the context lengths: lane l looks after
+// sequences [b0, b1); NL, NF and NP count the units of each class (x NG head groups); `above` is the
+// CTA's table of class-P sequences per tile-count bucket: above[t] = number of such sequences
+// whose partial partition falls in a bucket above t (built once per CTA).
+constexpr int kGroupLongPartitions = 8;
+
 struct GroupSched {
     int b0, b1;
-    long long excl_f, mine_f;   // full partitions of the sequences before / inside this lane's range
-    long long NF, NP;
+    long long excl_l, mine_l;   // class-L units (per head group) of the sequences before / inside this lane's range
+    long long excl_f, mine_f;   // class-F units (per head group), likewise
+    long long NL, NF, NP;
+    long long nonempty;         // sequences with at least one token
     int NG, TWc;                // head groups, top bucket
     const int* above;
 };
 
+// Partitions of a sequence of c tokens; whether it is long (class L).
+__device__ __forceinline__ int group_nv(int c, int W) { return (c + W - 1) / W; }
+__device__ __forceinline__ bool group_long(int c, int W) { return group_nv(c, W) >= kGroupLongPartitions; }
+
+// Class-P bucket of a sequence of c tokens (0: no class-P unit).
 __device__ __forceinline__ int group_bucket(int c, int W, int TWc) {
     const int rem = c % W;
-    return rem == 0 ? 0 : min((rem + 15) >> 4, TWc);
+    return (rem == 0 || group_long(c, W)) ? 0 : min((rem + 15) >> 4, TWc);
 }
 
 // The bucket table (whole CTA, after the grid-dependency wait; a __syncthreads must follow):
@@ -121,22 +139,32 @@ __device__ inline void group_sched_init(const DecodeArgs& a, GroupSched& s, cons
     s.NG = a.Hk / a.HG;
     s.TWc = min(a.W >> 4, kGroupBuckets);
     s.above = above;
-    long long nf = 0, np = 0;
+    long long nl = 0, nf = 0, np = 0, ne = 0;
     bool bad = false;
     for (int b = s.b0; b < s.b1; ++b) {
         const int raw = __ldg(a.context_lens + b);
         if (raw < 0 || raw > max_ctx) bad = true;
         const int c = sanitize_ctx(raw, max_ctx);
-        nf += c / a.W;
-        np += (c % a.W) != 0;
+        ne += c > 0;
+        if (group_long(c, a.W)) {
+            nl += group_nv(c, a.W);
+        } else {
+            nf += c / a.W;
+            np += (c % a.W) != 0;
+        }
     }
     if (report && bad && a.err_word) atomicOr(a.err_word, PDA_ERRW_BAD_CONTEXT_LEN);
-    long long tf, tp;
+    long long tl, tf, tp, te;
+    s.excl_l = warp_excl_scan(nl, tl);
     s.excl_f = warp_excl_scan(nf, tf);
     (void)warp_excl_scan(np, tp);
+    (void)warp_excl_scan(ne, te);
+    s.mine_l = nl;
     s.mine_f = nf;
+    s.NL = tl * s.NG;
     s.NF = tf * s.NG;
     s.NP = tp * s.NG;
+    s.nonempty = te;
 }
 
 // Unit k of the launch's order (whole warp; the result is warp-uniform).
@@ -145,22 +173,25 @@ __device__ inline GroupUnit group_unit(const DecodeArgs& a, const GroupSched& s,
     GroupUnit u;
     u.valid = false;
     u.b = u.g = u.p = u.ctx = 0;
-    if (k < 0 || k >= s.NF + s.NP) return u;
+    if (k < 0 || k >= s.NL + s.NF + s.NP) return u;
     int fb = -1, fg = 0, fp = 0, fc = 0;
-    if (k < s.NF) {
-        // full units in (sequence, head group, partition) order
-        const long long lo = s.excl_f * s.NG;
-        if (s.mine_f > 0 && lo <= k && k < lo + s.mine_f * s.NG) {
+    if (k < s.NL + s.NF) {
+        // classes L and F: (sequence, head group, partition) order over the class's sequences
+        const bool L = k < s.NL;
+        const long long kk = L ? k : k - s.NL;
+        const long long lo = (L ? s.excl_l : s.excl_f) * s.NG, mine = L ? s.mine_l : s.mine_f;
+        if (mine > 0 && lo <= kk && kk < lo + mine * s.NG) {
             long long pos = lo;
             for (int b = s.b0; b < s.b1; ++b) {
                 const int c = sanitize_ctx(__ldg(a.context_lens + b), max_ctx);
-                const long long n = (long long)(c / a.W) * s.NG;
-                if (k < pos + n) {
-                    const int nf = c / a.W;
-                    const int r = (int)(k - pos);
+                if (group_long(c, a.W) != L) continue;
+                const int nu = L ? group_nv(c, a.W) : c / a.W;   // units of one head group
+                const long long n = (long long)nu * s.NG;
+                if (kk < pos + n) {
+                    const int r = (int)(kk - pos);
                     fb = b;
-                    fg = r / nf;
-                    fp = r - fg * nf;
+                    fg = r / nu;
+                    fp = r - fg * nu;
                     fc = c;
                     break;
                 }
@@ -168,9 +199,9 @@ __device__ inline GroupUnit group_unit(const DecodeArgs& a, const GroupSched& s,
             }
         }
     } else {
-        // partial units by decreasing tile count (bucket), then sequence, then head group: the
-        // bucket from the CTA's table (the largest t with above[t] <= i), the sequence by one scan
-        const long long j = k - s.NF;
+        // class P by decreasing tile count (bucket), then sequence, then head group: the bucket
+        // from the CTA's table (the largest t with above[t] <= i), the sequence by one scan
+        const long long j = k - s.NL - s.NF;
         const int i = (int)(j / s.NG);
         int lo = 1, hi = s.TWc;   // above[] is non-increasing in t; above[TWc] = 0 <= i
         while (lo < hi) {
@@ -219,7 +250,7 @@ __device__ __forceinline__ long long group_take(const DecodeArgs& a) {
     return (long long)__shfl_sync(kFull, k, 0);
 }
 
-template <int NT, int S>
+template <int NT, int S, bool FUSED>
 struct GroupDecode {
     using D = Decode<PDA_KV_FP8_E4M3, NT, 3, false>;
     static constexpr int R = 4;   // unit descriptors in flight from the producer to the consumers
@@ -310,11 +341,14 @@ struct GroupDecode {
         if (lane == 0) {
             if (!ok && a.err_word) atomicOr(a.err_word, PDA_ERRW_PIPELINE_TIMEOUT);
             // this CTA takes no more units (its last take, or a wait that gave up, came first);
-            // the launch's last CTA to get here returns the counter pair to zero
-            __threadfence();
-            if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
-                a.sched[0] = 0u;
-                a.sched[1] = 0u;
+            // the launch's last CTA to get here returns the counter pair to zero (the fused step
+            // returns its counters to zero in group_exit instead)
+            if constexpr (!FUSED) {
+                __threadfence();
+                if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
+                    a.sched[0] = 0u;
+                    a.sched[1] = 0u;
+                }
             }
             // no copy may land in this CTA's memory after it leaves: wait (bounded, by the default
             // limit whatever the plan asked for) for the last copy issued into every stage
@@ -362,6 +396,8 @@ struct GroupDecode {
         }
         int cs = 0;
         uint32_t cph = 0;
+        GroupUnit done;   // fused step: the last unit whose partial this consumer wrote and has not yet reported
+        done.valid = false;
         for (long long i = 0; u.valid && ok; ++i) {
             const int h = u.g * HG + c;
             // ---- Q fragments: every bf16 bit of Q kept in f16 by a power-of-two scale
@@ -390,12 +426,16 @@ struct GroupDecode {
                         qf[n][kk][1] = pack_f16(bf16_lo(y) * pw, bf16_hi(y) * pw);
                     }
             }
-            // ---- the next unit's Q rows are requested now and land while this unit runs
+            // ---- the next unit's Q rows are requested while this unit runs: right away, or, in the
+            // fused step, after the previous unit's partial has been reported (the report's fence
+            // would otherwise wait for these loads)
             const GroupUnit nx = read_unit(m, i + 1, lane, ok, a.timeout_ns);
             if (!ok) break;
-            if (nx.valid) {
+            bool q_pending = nx.valid;
+            if (q_pending && !(FUSED && done.valid)) {
                 UnitIt ui{nx.b, nx.g * HG + c, nx.p, nx.ctx, 0, 0};
                 D::load_q(a, ui, qn, lane);
+                q_pending = false;
             }
 
             float acc[NT][8][4];
@@ -438,6 +478,15 @@ struct GroupDecode {
                         reinterpret_cast<const float*>(m.ptr + m.off_scales + s0 * scale_bytes + c * 128)};
                     const int vv[1] = {v0};
                     D::template step_fp8<1>(st, sc, vv, cq, qf, acc, m2, mt, ls, F, rF, lane);
+                }
+                if (FUSED && done.valid) {   // the previous unit's bulk copy has long completed by now
+                    report_done(a, done, lane);
+                    done.valid = false;
+                }
+                if (q_pending) {
+                    UnitIt ui{nx.b, nx.g * HG + c, nx.p, nx.ctx, 0, 0};
+                    D::load_q(a, ui, qn, lane);
+                    q_pending = false;
                 }
                 t += two ? 2 : 1;
                 // the stages go back to the producer once every lane's reads of them are done; the
@@ -528,11 +577,120 @@ struct GroupDecode {
                         }
                     }
             }
+            if constexpr (FUSED) done = u;
             u = nx;
         }
+        if (FUSED && done.valid && ok) report_done(a, done, lane);
         if (lane == 0) {
             if (!ok && a.err_word) atomicOr(a.err_word, PDA_ERRW_PIPELINE_TIMEOUT);
             bulk_wait_all();   // the partials are written before the CTA retires
+        }
+        __syncwarp();
+    }
+
+    // ------------------------------------------------------------------ fused step
+    // Counters of the fused step (caller's `counters`, int32 [B][Hk], zero at launch and left zero):
+    // for head group g of sequence b, entry (b*NG + g)*HG counts the partials written (one per
+    // consumer per unit; complete at nv*HG), and entry t*HG + 1 is the t-th slot of the queue of
+    // complete head groups (b*NG + g + 1; 0 = not yet pushed).  The launch's counter slot holds
+    // {next unit, -, queue tail, next row to merge, warps done}.
+
+    // This consumer's partial of unit u (and its statistics) is written: count it; the consumer
+    // that completes the head group queues it for merging.
+    static __device__ void report_done(const DecodeArgs& a, const GroupUnit& u, int lane) {
+        if (lane == 0) {
+            bulk_wait_all();              // the bulk copy of the partial has completed ...
+            fence_proxy_async_global();   // ... and is ordered before what follows
+        }
+        __threadfence();                  // every lane's statistics stores, before the count
+        __syncwarp();
+        if (lane == 0) {
+            const int NG = a.Hk / a.HG;
+            const int bg = u.b * NG + u.g;
+            const int nv = (u.ctx + a.W - 1) / a.W;
+            if (atomicAdd(a.counters + (long long)bg * a.HG, 1) == nv * a.HG - 1) {
+                __threadfence();
+                const unsigned int t = atomicAdd(a.sched + 2, 1u);
+                st_release_gpu(a.counters + (long long)t * a.HG + 1, bg + 1);
+            }
+        }
+        __syncwarp();
+    }
+
+    // Merges queued rows until every row of the launch has been taken.  Rows are numbered in
+    // queue order, HG*QG per head group; a row whose head group is not yet queued is waited for
+    // (bounded): only CTAs already running hold units, so the wait ends.
+    static __device__ void merge_rows(const DecodeArgs& a, const GroupSched& s, int lane, bool& ok) {
+        const int HG = a.HG, NG = a.Hk / a.HG, rows_per_group = a.HG * a.QG;
+        const long long total = s.nonempty * a.Hk * a.QG;
+        const MergeArgs mg{a.partial_out, a.exp_sums, a.max_logits, a.out, a.Hk, a.QG, a.P, a.W, a.out_f32};
+        while (ok) {
+            unsigned int rc = 0;
+            if (lane == 0) rc = atomicAdd(a.sched + 3, 1u);
+            rc = __shfl_sync(kFull, rc, 0);
+            if ((long long)rc >= total) break;
+            const unsigned int t = rc / rows_per_group, r = rc - t * rows_per_group;
+            int v = 0;
+            if (lane == 0) {
+                const int* slot = a.counters + (long long)t * HG + 1;
+                const uint64_t t0 = global_timer_ns();
+                unsigned int backoff = 32;
+                while ((v = ld_acquire_gpu(slot)) == 0) {
+                    if (global_timer_ns() - t0 > a.timeout_ns) break;
+                    __nanosleep(backoff);
+                    backoff = min(backoff * 2, 1024u);
+                }
+            }
+            v = __shfl_sync(kFull, v, 0);
+            if (v == 0) {
+                ok = false;
+                break;
+            }
+            const int bg = v - 1, b = bg / NG, g = bg - (bg / NG) * NG;
+            const int h = g * HG + (int)(r / a.QG), q = (int)(r % a.QG);
+            merge_row(mg, b, h, q, sanitize_ctx(a.context_lens[b], a.MB * a.BS));
+        }
+    }
+
+    // Rows of sequences without tokens (and of out-of-range lengths) are zero; sequence b falls
+    // to CTA b mod grid.
+    static __device__ void zero_empty_rows(const DecodeArgs& a, int lane) {
+        const long long rows = (long long)a.Hk * a.QG;
+        for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
+            if (sanitize_ctx(__ldg(a.context_lens + b), a.MB * a.BS) != 0) continue;
+            for (long long rr = 0; rr < rows; ++rr) {
+                const long long orow = (long long)b * rows + rr;
+                if (a.out_f32) {
+                    reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * kHeadDim)[lane] =
+                        make_float4(0.f, 0.f, 0.f, 0.f);
+                } else {
+                    reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow * kHeadDim)[lane] = make_uint2(0u, 0u);
+                }
+            }
+        }
+    }
+
+    // Every warp of the launch ends here; the last one returns the counters to zero.
+    static __device__ void group_exit(const DecodeArgs& a, bool ok, int lane) {
+        if (!ok && lane == 0 && a.err_word) atomicOr(a.err_word, PDA_ERRW_PIPELINE_TIMEOUT);
+        __threadfence();
+        __syncwarp();
+        unsigned int old = 0;
+        if (lane == 0) old = atomicAdd(a.sched + 4, 1u);
+        old = __shfl_sync(kFull, old, 0);
+        const unsigned int warps = gridDim.x * (blockDim.x >> 5);
+        if (old != warps - 1) return;
+        __threadfence();
+        const long long groups = (long long)a.B * (a.Hk / a.HG);
+        for (long long i = lane; i < groups; i += 32) {
+            a.counters[i * a.HG] = 0;
+            a.counters[i * a.HG + 1] = 0;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            a.sched[0] = a.sched[1] = a.sched[2] = a.sched[3] = 0u;
+            __threadfence();
+            a.sched[4] = 0u;
         }
         __syncwarp();
     }
@@ -571,22 +729,38 @@ struct GroupDecode {
         grid_dependency_wait();     // inputs may come from the previous grid on the stream
         group_buckets_init(a, above, hist);
         __syncthreads();            // the barriers and the bucket table are ready
-        if (warp == 0)
-            produce(a, kv_map, sc_map, m);
-        else if (warp <= HG)
-            consume(a, warp - 1, m);
+        if constexpr (!FUSED) {
+            if (warp == 0)
+                produce(a, kv_map, sc_map, m);
+            else if (warp <= HG)
+                consume(a, warp - 1, m);
+        } else {
+            // producer, consumers, and one warp that merges from the start; the others merge too
+            // once they have no unit left
+            if (warp == 0)
+                produce(a, kv_map, sc_map, m);
+            else if (warp <= HG)
+                consume(a, warp - 1, m);
+            else
+                zero_empty_rows(a, lane);
+            GroupSched s;
+            group_sched_init(a, s, m.above, false);
+            bool ok = true;
+            merge_rows(a, s, lane, ok);
+            group_exit(a, ok, lane);
+        }
     }
 };
 
 // NWARPS: warps per CTA the register allocation is sized for (producer + up to NWARPS - 1
 // consumers); MINB: CTAs per SM it must allow.
-template <int NT, int S, int NWARPS, int MINB>
+template <int NT, int S, int NWARPS, int MINB, bool FUSED>
 __global__ void __launch_bounds__(NWARPS * 32, MINB) pda_group_kernel(const __grid_constant__ CUtensorMap kv_map,
                                                                      const __grid_constant__ CUtensorMap sc_map,
                                                                      const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    GroupDecode<NT, S>::run(a, &kv_map, &sc_map, smem);
+    GroupDecode<NT, S, FUSED>::run(a, &kv_map, &sc_map, smem);
 }
 
 }  // namespace pda

@@ -26,8 +26,8 @@ struct DecodeArgs {
     int B, Hk, QG, MB, BS, P, W;
     int bs_shift;              // log2(BS)
     int HG;                    // head-group kernel: KV heads per CTA (a divisor of Hk, <= 4)
-    unsigned int* sched;       // head-group kernel: this launch's {next unit, CTAs done} counter pair,
-                               // zero at launch and left zero by the launch's last CTA
+    unsigned int* sched;       // head-group kernel: this launch's slot of counters, zero at launch
+                               // and left zero by the launch's last CTA (or warp, fused step)
     float qk_scale_log2;       // softmax_scale * log2(e)
     unsigned long long timeout_ns;
     // fused step only: per-(sequence, KV head) arrival counters and the final output
@@ -52,8 +52,10 @@ int launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& kv_map, bool fuse
 int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, bool fused,
                       cudaStream_t stream);
 // The head-group kernel (fp8): a.HG heads per CTA; the maps' boxes span a.HG heads.
+// With `fused`, the same launch also combines the partials into `out` (a.counters as the fused
+// step's counters; a.HG >= 2).
 int launch_decode_fp8_groups(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
-                             cudaStream_t stream);
+                             bool fused, cudaStream_t stream);
 // KV heads per CTA of the head-group kernel for Hk heads: the largest divisor of Hk not above 4.
 int group_heads(int Hk);
 int launch_decode_tq4(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, cudaStream_t stream);

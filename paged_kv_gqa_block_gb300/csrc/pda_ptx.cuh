@@ -106,6 +106,13 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// Bulk copy global -> shared of `bytes` (16-byte aligned addresses, a multiple of 16 bytes),
+// completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 // Bulk copy shared -> global of `bytes` (16-byte aligned addresses, a multiple of 16 bytes),
 // tracked by this thread's bulk groups.
 __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
@@ -202,6 +209,19 @@ __device__ __forceinline__ float partition_weight(float l_p, float m_p, float M)
     return __fmul_rn(l_p, ex2(__fmul_rn(__fsub_rn(m_p, M), 1.4426950408889634f)));
 }
 
+// Orders the global-memory writes of this thread's completed bulk copies (async proxy) before its
+// later generic-proxy accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 // Orders this thread's earlier generic-proxy shared-memory accesses before later async-proxy
 // (TMA) accesses to the same memory.
 __device__ __forceinline__ void fence_proxy_async_shared() {

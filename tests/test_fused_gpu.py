@@ -21,9 +21,9 @@ def pda():
     return pda
 
 
-def run_both(pda, inp, G=None, repeats=2):
+def run_both(pda, inp, G=None, repeats=2, variant=0):
     w = inp.workload
-    p = plan_for(w, G)
+    p = plan_for(w, G, variant)
     d = to_device(inp)
     shape = (w.num_seqs, w.num_q_heads, 128)
     two = torch.empty(shape, dtype=torch.float32, device="cuda")
@@ -58,12 +58,22 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("kv,QG,BS,G,Hk,ctx", CASES)
-def test_fused_matches_oracle_and_the_two_launch_path(oracle_mod, pda, kv, QG, BS, G, Hk, ctx):
+CASES += [
+    # the fused head-group step: groups of 4 (one and two per sequence), 2 and 3 heads, 79 partitions
+    (wl.KV_FP8_E4M3, 6, 16, 1, 8, (1, 17, 300, 2048, 5000, 0, 4097)),
+    (wl.KV_FP8_E4M3, 8, 32, 1, 4, (20000, 1, 0, 255)),
+    (wl.KV_FP8_E4M3, 16, 16, 2, 2, (513, 2000, 1)),
+    (wl.KV_FP8_E4M3, 6, 32, 5, 6, (1281, 40, 3000, 0)),
+]
+FUSED_CASES = [(*c, v) for c in CASES for v in ((1, 2) if c[0] == wl.KV_FP8_E4M3 else (0,))]
+
+
+@pytest.mark.parametrize("kv,QG,BS,G,Hk,ctx,variant", FUSED_CASES)
+def test_fused_matches_oracle_and_the_two_launch_path(oracle_mod, pda, kv, QG, BS, G, Hk, ctx, variant):
     w = wl.small(num_seqs=len(ctx), num_kv_heads=Hk, query_group_size=QG, kv_block_size=BS, ctx=ctx, kv_dtype=kv,
                  tile_groups_per_partition=G, seed=200 + QG + BS + G, extra_blocks=5)
     inp = wl.generate(w)
-    two, fused = run_both(pda, inp)
+    two, fused = run_both(pda, inp, variant=variant)
     ref = oh.run_oracle(inp, G=G)["out"]
     tol = TOL[kv]
     for k, o in enumerate(fused):
@@ -74,15 +84,15 @@ def test_fused_matches_oracle_and_the_two_launch_path(oracle_mod, pda, kv, QG, B
             assert np.all(np.abs(o - ref) <= tol + bf16_half_ulp(ref))
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
-def test_fused_bad_context_length_sets_the_bit_and_zeroes_that_sequence(oracle_mod, pda, kv):
-    w = wl.small(num_seqs=3, num_kv_heads=2, ctx=(300, 20, 33), kv_dtype=kv, seed=38)
+@pytest.mark.parametrize("kv,variant", [(wl.KV_BF16, 0), (wl.KV_FP8_E4M3, 1), (wl.KV_FP8_E4M3, 2)])
+def test_fused_bad_context_length_sets_the_bit_and_zeroes_that_sequence(oracle_mod, pda, kv, variant):
+    w = wl.small(num_seqs=3, num_kv_heads=4, ctx=(300, 20, 33), kv_dtype=kv, seed=38)
     inp = wl.generate(w)
     ref = oh.run_oracle(inp)["out"]
     ctx = inp.context_lens.copy()
     ctx[1] = -5
     d = to_device(wl.Inputs(w, inp.query, inp.cache, inp.block_table, ctx))
-    p = plan_for(w)
+    p = plan_for(w, variant=variant)
     ws = pda.workspace(p, "cuda")
     cnt = pda.counters(p, "cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -98,20 +108,46 @@ def test_fused_bad_context_length_sets_the_bit_and_zeroes_that_sequence(oracle_m
     assert int(cnt.abs().sum().item()) == 0
 
 
-@pytest.mark.parametrize("name", ["b8_hk8_qg8_bs16_ctx1-4096", "b64_hk8_qg6_bs16_fp8_lognormal2048"])
-def test_fused_full_size_equals_two_launch(pda, name):
+@pytest.mark.parametrize("name,variant", [("b8_hk8_qg8_bs16_ctx1-4096", 0), ("b64_hk8_qg6_bs16_fp8_lognormal2048", 1),
+                                          ("b64_hk8_qg6_bs16_fp8_lognormal2048", 2)])
+def test_fused_full_size_equals_two_launch(pda, name, variant):
     inp = wl.generate(wl.WORKLOADS[name])
-    two, fused = run_both(pda, inp, repeats=1)
-    assert np.array_equal(fused[0], two)
+    two, fused = run_both(pda, inp, repeats=2, variant=variant)
+    for o in fused[::2]:
+        assert np.array_equal(o, two)
 
 
-@pytest.mark.parametrize("kv", [wl.KV_BF16, wl.KV_FP8_E4M3])
-def test_fused_repeat_runs_are_bitwise_identical(pda, kv):
-    # the fused step's merge runs in whichever warp arrives last, but always in partition order
-    w = wl.small(num_seqs=4, num_kv_heads=2, ctx=(1000, 3, 513, 2000), seed=36, kv_dtype=kv)
+def test_fused_head_groups_counters_return_to_zero_across_many_launches(oracle_mod, pda):
+    # the fused head-group step takes a counter slot per launch (256 of them) and leaves its slot
+    # and the caller's counters at zero: 600 launches in a row give the first launch's bits
+    w = wl.small(num_seqs=5, num_kv_heads=8, query_group_size=6, kv_block_size=16, ctx=(3000, 17, 0, 1200, 256),
+                 kv_dtype=wl.KV_FP8_E4M3, seed=97)
     inp = wl.generate(w)
     d = to_device(inp)
-    p = plan_for(w)
+    p = plan_for(w, variant=2)
+    ws = pda.workspace(p, "cuda")
+    cnt = pda.counters(p, "cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    shape = (w.num_seqs, w.num_q_heads, 128)
+    first = torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
+    last = torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
+    for i in range(600):
+        o = first if i == 0 else last
+        pda.decode_fused(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"],
+                         ws["partial_out"], ws["exp_sums"], ws["max_logits"], cnt, o, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and int(cnt.abs().sum().item()) == 0
+    assert torch.equal(first, last)
+    assert np.abs(first.cpu().numpy() - oh.run_oracle(inp)["out"]).max() <= TOL[wl.KV_FP8_E4M3]
+
+
+@pytest.mark.parametrize("kv,variant", [(wl.KV_BF16, 0), (wl.KV_FP8_E4M3, 1), (wl.KV_FP8_E4M3, 2)])
+def test_fused_repeat_runs_are_bitwise_identical(pda, kv, variant):
+    # the fused step's merges run in whichever warp takes them, but always in partition order
+    w = wl.small(num_seqs=4, num_kv_heads=4, ctx=(1000, 3, 513, 2000), seed=36, kv_dtype=kv)
+    inp = wl.generate(w)
+    d = to_device(inp)
+    p = plan_for(w, variant=variant)
     ws = pda.workspace(p, "cuda")
     cnt = pda.counters(p, "cuda")
     outs, parts = [], []
