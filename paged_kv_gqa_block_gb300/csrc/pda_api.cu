@@ -294,10 +294,7 @@ static int decode_launch(const pda_plan_t* plan, const void* query, const void* 
     a.sched = nullptr;
     CUtensorMap kv_map, sc_map;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the fused step runs on head groups when they hold at least two heads (its counters need two
-    // entries per group), else on head warps
-    if (plan->kv_dtype == PDA_KV_FP8_E4M3 && use_head_groups(plan) &&
-        (!fused || group_heads(plan->num_kv_heads) >= 2)) {
+    if (plan->kv_dtype == PDA_KV_FP8_E4M3 && use_head_groups(plan)) {
         a.HG = group_heads(plan->num_kv_heads);
         if (!encode_kv_map(&kv_map, kv_cache, plan, num_cache_blocks, a.HG) ||
             !encode_scale_map(&sc_map, kv_cache, plan, num_cache_blocks, a.HG))

@@ -24,9 +24,8 @@ int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUte
 }
 
 // Counters of the head-group kernel: kSchedSlots slots of kSchedInts counters ({next unit,
-// producers done} for the partition pass; {next unit, -, queue tail, next row, warps done} for the
-// fused step), every slot zero between launches (each launch's last CTA or warp returns its slot
-// to zero).  Each launch takes the next slot in turn, so launches in flight at the same time (on
+// producers done} for the partition pass; {next unit, -, -, -, CTAs done} for the fused step),
+// every slot zero between launches (each launch's last CTA returns its slot to zero).  Each launch takes the next slot in turn, so launches in flight at the same time (on
 // other streams) use different slots as long as fewer than kSchedSlots of them overlap.  The array
 // lives in every GPU that loads the library.
 constexpr int kSchedSlots = 256, kSchedInts = 8;
@@ -75,7 +74,7 @@ static int launch_groups(const DecodeArgs& a, const CUtensorMap& kv_map, const C
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PDA_ERR_CUDA;
     const int threads = 32 * (a.HG + (FUSED ? 2 : 1));   // producer, HG consumers (, merger)
     const int smem = group_smem_bytes(a.HG, S);
-    if (a.HG < 1 || threads > 32 * NWARPS || (FUSED && a.HG < 2)) return PDA_ERR_INVALID_ARG;
+    if (a.HG < 1 || threads > 32 * NWARPS) return PDA_ERR_INVALID_ARG;
     int occ;
     {
         std::lock_guard<std::mutex> lock(mu);

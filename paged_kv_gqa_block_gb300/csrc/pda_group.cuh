@@ -342,7 +342,7 @@ struct GroupDecode {
             if (!ok && a.err_word) atomicOr(a.err_word, PDA_ERRW_PIPELINE_TIMEOUT);
             // this CTA takes no more units (its last take, or a wait that gave up, came first);
             // the launch's last CTA to get here returns the counter pair to zero (the fused step
-            // returns its counters to zero in group_exit instead)
+            // returns its counters to zero at its end instead)
             if constexpr (!FUSED) {
                 __threadfence();
                 if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
@@ -590,13 +590,11 @@ struct GroupDecode {
 
     // ------------------------------------------------------------------ fused step
     // Counters of the fused step (caller's `counters`, int32 [B][Hk], zero at launch and left zero):
-    // for head group g of sequence b, entry (b*NG + g)*HG counts the partials written (one per
-    // consumer per unit; complete at nv*HG), and entry t*HG + 1 is the t-th slot of the queue of
-    // complete head groups (b*NG + g + 1; 0 = not yet pushed).  The launch's counter slot holds
-    // {next unit, -, queue tail, next row to merge, warps done}.
+    // entry b*NG + g counts the partials of head group g of sequence b that are written (one per
+    // consumer per unit; complete at nv*HG).  The launch's counter slot holds {next unit, -, -, -,
+    // CTAs done}.
 
-    // This consumer's partial of unit u (and its statistics) is written: count it; the consumer
-    // that completes the head group queues it for merging.
+    // This consumer's partial of unit u (and its statistics) is written: count it.
     static __device__ void report_done(const DecodeArgs& a, const GroupUnit& u, int lane) {
         if (lane == 0) {
             bulk_wait_all();              // the bulk copy of the partial has completed ...
@@ -604,97 +602,54 @@ struct GroupDecode {
         }
         __threadfence();                  // every lane's statistics stores, before the count
         __syncwarp();
-        if (lane == 0) {
-            const int NG = a.Hk / a.HG;
-            const int bg = u.b * NG + u.g;
-            const int nv = (u.ctx + a.W - 1) / a.W;
-            if (atomicAdd(a.counters + (long long)bg * a.HG, 1) == nv * a.HG - 1) {
-                __threadfence();
-                const unsigned int t = atomicAdd(a.sched + 2, 1u);
-                st_release_gpu(a.counters + (long long)t * a.HG + 1, bg + 1);
-            }
-        }
+        if (lane == 0) atomicAdd(a.counters + (long long)u.b * (a.Hk / a.HG) + u.g, 1);
         __syncwarp();
     }
 
-    // Merges queued rows until every row of the launch has been taken.  Rows are numbered in
-    // queue order, HG*QG per head group; a row whose head group is not yet queued is waited for
-    // (bounded): only CTAs already running hold units, so the wait ends.
-    static __device__ void merge_rows(const DecodeArgs& a, const GroupSched& s, int lane, bool& ok) {
-        const int HG = a.HG, NG = a.Hk / a.HG, rows_per_group = a.HG * a.QG;
-        const long long total = s.nonempty * a.Hk * a.QG;
+    // Merges this warp's share of the output rows (b, h, q), in row order.  Rows of long sequences
+    // (complete early, while the pass still streams) go to the CTAs' merger warps, dealt round robin;
+    // the other rows (complete near the end) to every warp of the launch.  A row waits (bounded)
+    // until every partial of its head group is counted: only CTAs already running hold units, so
+    // the wait ends.  Rows of sequences without tokens are written as zeros.
+    static __device__ void merge_rows(const DecodeArgs& a, bool merger, int lane, bool& ok) {
+        const int max_ctx = a.MB * a.BS, NG = a.Hk / a.HG, nwarps = blockDim.x >> 5;
+        const long long rows = (long long)a.B * a.Hk * a.QG;
+        const long long mstride = gridDim.x, mfirst = blockIdx.x;                       // merger warps
+        const long long astride = (long long)gridDim.x * nwarps,
+                        afirst = (long long)blockIdx.x * nwarps + (threadIdx.x >> 5);  // every warp
         const MergeArgs mg{a.partial_out, a.exp_sums, a.max_logits, a.out, a.Hk, a.QG, a.P, a.W, a.out_f32};
-        while (ok) {
-            unsigned int rc = 0;
-            if (lane == 0) rc = atomicAdd(a.sched + 3, 1u);
-            rc = __shfl_sync(kFull, rc, 0);
-            if ((long long)rc >= total) break;
-            const unsigned int t = rc / rows_per_group, r = rc - t * rows_per_group;
-            int v = 0;
-            if (lane == 0) {
-                const int* slot = a.counters + (long long)t * HG + 1;
-                const uint64_t t0 = global_timer_ns();
-                unsigned int backoff = 32;
-                while ((v = ld_acquire_gpu(slot)) == 0) {
-                    if (global_timer_ns() - t0 > a.timeout_ns) break;
-                    __nanosleep(backoff);
-                    backoff = min(backoff * 2, 1024u);
+        for (int pass = 0; pass < 2 && ok; ++pass) {
+            if (pass == 0 && !merger) continue;
+            const long long first = pass == 0 ? mfirst : afirst, stride = pass == 0 ? mstride : astride;
+            for (long long row = first; row < rows && ok; row += stride) {
+                const long long unit = row / a.QG;
+                const int q = (int)(row - unit * a.QG);
+                const int b = (int)(unit / a.Hk), h = (int)(unit - (long long)b * a.Hk);
+                const int c = sanitize_ctx(__ldg(a.context_lens + b), max_ctx);
+                if (group_long(c, a.W) != (pass == 0)) continue;
+                const int nv = group_nv(c, a.W);
+                if (nv > 0) {
+                    int seen = 0;
+                    if (lane == 0) {
+                        const int* cnt = a.counters + (long long)b * NG + h / a.HG;
+                        const uint64_t t0 = global_timer_ns();
+                        unsigned int backoff = 64;
+                        while ((seen = ld_acquire_gpu(cnt)) < nv * a.HG) {
+                            if (global_timer_ns() - t0 > a.timeout_ns) break;
+                            __nanosleep(backoff);
+                            backoff = min(backoff * 2, 1024u);
+                        }
+                    }
+                    seen = __shfl_sync(kFull, seen, 0);
+                    if (seen < nv * a.HG) {
+                        ok = false;
+                        break;
+                    }
                 }
-            }
-            v = __shfl_sync(kFull, v, 0);
-            if (v == 0) {
-                ok = false;
-                break;
-            }
-            const int bg = v - 1, b = bg / NG, g = bg - (bg / NG) * NG;
-            const int h = g * HG + (int)(r / a.QG), q = (int)(r % a.QG);
-            merge_row(mg, b, h, q, sanitize_ctx(a.context_lens[b], a.MB * a.BS));
-        }
-    }
-
-    // Rows of sequences without tokens (and of out-of-range lengths) are zero; sequence b falls
-    // to CTA b mod grid.
-    static __device__ void zero_empty_rows(const DecodeArgs& a, int lane) {
-        const long long rows = (long long)a.Hk * a.QG;
-        for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
-            if (sanitize_ctx(__ldg(a.context_lens + b), a.MB * a.BS) != 0) continue;
-            for (long long rr = 0; rr < rows; ++rr) {
-                const long long orow = (long long)b * rows + rr;
-                if (a.out_f32) {
-                    reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * kHeadDim)[lane] =
-                        make_float4(0.f, 0.f, 0.f, 0.f);
-                } else {
-                    reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow * kHeadDim)[lane] = make_uint2(0u, 0u);
-                }
+                merge_row(mg, b, h, q, c);
             }
         }
     }
-
-    // Every warp of the launch ends here; the last one returns the counters to zero.
-    static __device__ void group_exit(const DecodeArgs& a, bool ok, int lane) {
-        if (!ok && lane == 0 && a.err_word) atomicOr(a.err_word, PDA_ERRW_PIPELINE_TIMEOUT);
-        __threadfence();
-        __syncwarp();
-        unsigned int old = 0;
-        if (lane == 0) old = atomicAdd(a.sched + 4, 1u);
-        old = __shfl_sync(kFull, old, 0);
-        const unsigned int warps = gridDim.x * (blockDim.x >> 5);
-        if (old != warps - 1) return;
-        __threadfence();
-        const long long groups = (long long)a.B * (a.Hk / a.HG);
-        for (long long i = lane; i < groups; i += 32) {
-            a.counters[i * a.HG] = 0;
-            a.counters[i * a.HG + 1] = 0;
-        }
-        __syncwarp();
-        if (lane == 0) {
-            a.sched[0] = a.sched[1] = a.sched[2] = a.sched[3] = 0u;
-            __threadfence();
-            a.sched[4] = 0u;
-        }
-        __syncwarp();
-    }
-
     static __device__ void run(const DecodeArgs& a, const CUtensorMap* kv_map, const CUtensorMap* sc_map,
                                uint8_t* smem) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -735,19 +690,34 @@ struct GroupDecode {
             else if (warp <= HG)
                 consume(a, warp - 1, m);
         } else {
-            // producer, consumers, and one warp that merges from the start; the others merge too
-            // once they have no unit left
+            // producer, consumers, and one warp that merges from the start; the others merge their
+            // share of the rows once they have no unit left
             if (warp == 0)
                 produce(a, kv_map, sc_map, m);
             else if (warp <= HG)
                 consume(a, warp - 1, m);
-            else
-                zero_empty_rows(a, lane);
-            GroupSched s;
-            group_sched_init(a, s, m.above, false);
             bool ok = true;
-            merge_rows(a, s, lane, ok);
-            group_exit(a, ok, lane);
+            merge_rows(a, warp == HG + 1, lane, ok);
+            if (!ok && lane == 0 && a.err_word) atomicOr(a.err_word, PDA_ERRW_PIPELINE_TIMEOUT);
+            // the launch's last CTA returns the counters to zero
+            __syncthreads();
+            if (warp == 0) {
+                __threadfence();
+                unsigned int old = 0;
+                if (lane == 0) old = atomicAdd(a.sched + 4, 1u);
+                old = __shfl_sync(kFull, old, 0);
+                if (old == gridDim.x - 1) {
+                    __threadfence();
+                    const long long groups = (long long)a.B * (a.Hk / a.HG);
+                    for (long long i = lane; i < groups; i += 32) a.counters[i] = 0;
+                    __syncwarp();
+                    if (lane == 0) {
+                        a.sched[0] = a.sched[1] = a.sched[2] = a.sched[3] = 0u;
+                        __threadfence();
+                        a.sched[4] = 0u;
+                    }
+                }
+            }
         }
     }
 };

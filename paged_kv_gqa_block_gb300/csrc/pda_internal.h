@@ -53,7 +53,7 @@ int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUte
                       cudaStream_t stream);
 // The head-group kernel (fp8): a.HG heads per CTA; the maps' boxes span a.HG heads.
 // With `fused`, the same launch also combines the partials into `out` (a.counters as the fused
-// step's counters; a.HG >= 2).
+// step's counters).
 int launch_decode_fp8_groups(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
                              bool fused, cudaStream_t stream);
 // KV heads per CTA of the head-group kernel for Hk heads: the largest divisor of Hk not above 4.
