@@ -359,7 +359,7 @@ def event_times(fn, n, flush, stream, before=None):
     return [a.elapsed_time(b) * 1e-3 for a, b in ev]
 
 
-def rates(w, inp, p, mean_step, mean_dec, world, peak, peaks):
+def rates(w, inp, p, mean_step, mean_dec, world, peak, peaks, kernel="pda_partition_kernel"):
     ab = algorithmic_bytes(w, inp.context_lens, p.partition_tokens)
     achieved = ab["decode"] / mean_dec / 1e9
     kv_gbs = ab["kv"] / mean_step / 1e9
@@ -369,7 +369,7 @@ def rates(w, inp, p, mean_step, mean_dec, world, peak, peaks):
         "kv_read_frac_of_measured": kv_gbs / peak,
         "decode_ms": mean_dec * 1e3,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": committed_traffic(w.name), "kernel": "pda_partition_kernel",
+                     "traffic": committed_traffic(w.name), "kernel": kernel,
                      "algorithmic_bytes_per_launch": ab["decode"],
                      "peak_source": "measured" if peaks else "fallback"},
     }
@@ -501,7 +501,7 @@ def run_ours(args, rank, world, local_rank):
             ms, md = sum(ts) / len(ts), sum(td) / len(td)
             if dist:
                 ms, md = max_over_ranks(dist, [ms, md], dev)
-            _, r = rates(wo, io, So.p, ms, md, world, peak, peaks)
+            _, r = rates(wo, io, So.p, ms, md, world, peak, peaks, kernel_name(pda, So.p))
             others.append({"workload": name, "kv_dtype": KV_NAMES[wo.kv_dtype], "steps": n_other,
                            "value": replica_throughput(world, So.units, ms), "unit": UNIT,
                            "ms_per_step": ms * 1e3, "step_ms_median": float(np.median(ts)) * 1e3, **r})
@@ -513,7 +513,7 @@ def run_ours(args, rank, world, local_rank):
             dist.destroy_process_group()
         return
 
-    ab, r = rates(w, inp, p, mean_step, mean_dec, world, peak, peaks)
+    ab, r = rates(w, inp, p, mean_step, mean_dec, world, peak, peaks, kernel_name(pda, p))
     res = {
         "metric": METRIC, "value": replica_throughput(world, units, mean_step), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_step * 1e3,
@@ -554,6 +554,11 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(res))
     if dist:
         dist.destroy_process_group()
+
+
+def kernel_name(pda, p) -> str:
+    """The partition kernel pda_decode launches for plan p (its roofline is the line's)."""
+    return "pda_group_kernel" if pda.kernel_variant(p) == pda.VARIANT_HEAD_GROUPS else "pda_partition_kernel"
 
 
 def e2e_in_bytes(inp) -> int:

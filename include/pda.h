@@ -263,6 +263,15 @@ PDA_API int pda_decode_step_noalloc(const pda_plan_t* plan, const void* query, c
                                     long long num_cache_blocks, const int* block_table, const int* context_lens,
                                     void* out, int out_dtype, int* err_word, void* stream);
 
+/*
+ * pda_kernel_variant -- host only; launches nothing.  The partition-pass layout pda_decode would
+ * launch for this plan on the current device: PDA_VARIANT_HEAD_WARPS or PDA_VARIANT_HEAD_GROUPS
+ * (plan->kernel_variant resolved, PDA_VARIANT_AUTO included).  Returns PDA_ERR_INVALID_ARG for
+ * a NULL or edited plan, PDA_ERR_CUDA when the device cannot be queried.  No counterpart on the
+ * pages.
+ */
+PDA_API int pda_kernel_variant(const pda_plan_t* plan);
+
 /* Human-readable name of a pda_status value (static string; never NULL). */
 PDA_API const char* pda_status_string(int status);
 

@@ -97,6 +97,8 @@ def lib():
             L.pda_decode_step_noalloc.argtypes = [P, _VP, _VP, ctypes.c_longlong, _VP, _VP, _VP, ctypes.c_int, _VP,
                                                   _VP]
             L.pda_decode_step_noalloc.restype = ctypes.c_int
+            L.pda_kernel_variant.argtypes = [P]
+            L.pda_kernel_variant.restype = ctypes.c_int
             L.pda_plan_struct_size.argtypes = []
             L.pda_plan_struct_size.restype = ctypes.c_int
             if L.pda_plan_struct_size() != ctypes.sizeof(Plan):
@@ -119,6 +121,15 @@ def plan(num_seqs: int, num_kv_heads: int, query_group_size: int, kv_block_size:
     if rc != 0:
         raise PdaError(rc, "pda_plan")
     return p
+
+
+def kernel_variant(p: Plan) -> int:
+    """pda_kernel_variant: the partition-pass layout pda_decode launches for this plan on the
+    current device (VARIANT_HEAD_WARPS or VARIANT_HEAD_GROUPS)."""
+    rc = lib().pda_kernel_variant(ctypes.byref(p))
+    if rc < 0:
+        raise PdaError(rc, "pda_kernel_variant")
+    return rc
 
 
 def partial_shapes(p: Plan):

@@ -381,4 +381,11 @@ long long pda_workspace_size(const pda_plan_t* plan) {
 
 int pda_plan_struct_size(void) { return (int)sizeof(pda_plan_t); }
 
+int pda_kernel_variant(const pda_plan_t* plan) {
+    if (!plan || !plan_matches(plan)) return PDA_ERR_INVALID_ARG;
+    if (plan->kv_dtype != PDA_KV_FP8_E4M3) return PDA_VARIANT_HEAD_WARPS;
+    if (plan->kernel_variant == PDA_VARIANT_AUTO && device_sm_count() <= 0) return PDA_ERR_CUDA;
+    return use_head_groups(plan) ? PDA_VARIANT_HEAD_GROUPS : PDA_VARIANT_HEAD_WARPS;
+}
+
 }  // extern "C"

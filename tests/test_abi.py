@@ -141,3 +141,16 @@ def test_head_group_variant_is_accepted_for_fp8(pda):
     for v in (0, 1, 2):
         p = pda.plan(2, 8, 6, 16, 4, kv_dtype=pda.KV_FP8_E4M3, kernel_variant=v)
         assert p.kernel_variant == v
+
+
+def test_kernel_variant_of_a_plan(pda):
+    L = pda.lib()
+    assert L.pda_kernel_variant(None) == -1
+    p = pda.plan(2, 8, 6, 16, 4, kv_dtype=pda.KV_BF16)
+    assert pda.kernel_variant(p) == pda.VARIANT_HEAD_WARPS            # head groups are fp8 only
+    for v, want in ((1, pda.VARIANT_HEAD_WARPS), (2, pda.VARIANT_HEAD_GROUPS)):
+        p = pda.plan(2, 8, 6, 16, 4, kv_dtype=pda.KV_FP8_E4M3, kernel_variant=v)
+        assert pda.kernel_variant(p) == want
+    edited = pda.Plan.from_buffer_copy(p)
+    edited.num_partitions += 1
+    assert L.pda_kernel_variant(ctypes.byref(edited)) == -1

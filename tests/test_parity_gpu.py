@@ -401,3 +401,14 @@ def test_head_group_counters_return_to_zero_across_many_launches(oracle_mod):
     assert int(err.item()) == 0
     assert np.array_equal(outs[0].view(np.int32), outs[1].view(np.int32))
     assert np.abs(outs[0] - oh.run_oracle(inp)["out"]).max() <= TOL[wl.KV_FP8_E4M3]
+
+
+def test_automatic_variant_on_the_full_size_workloads():
+    # the fp8 configuration (64 sequences, 8 heads: head groups of 4, 256 units of room per group)
+    # runs on head groups; every other format runs on head warps
+    import paged_kv_gqa_block_gb300 as pda
+    from tests.gpu_helpers import plan_for
+    for name in wl.WORKLOAD_ORDER:
+        w = wl.WORKLOADS[name]
+        want = pda.VARIANT_HEAD_GROUPS if w.kv_dtype == wl.KV_FP8_E4M3 else pda.VARIANT_HEAD_WARPS
+        assert pda.kernel_variant(plan_for(w)) == want, name
