@@ -20,12 +20,13 @@
  *   - Pointers named "device" are device pointers owned by the caller; the library allocates
  *     nothing, frees nothing and keeps no per-call state.  Process-wide state: a cache of the
  *     driver's tensor-map encoder and of per-device occupancy figures, and, in every GPU that
- *     loads the library, two small static arrays: 256 pairs of unit counters used by the fp8
- *     head-group kernel (each launch takes the next pair; the launch's last CTA returns it to
- *     zero, so a captured launch can be replayed; fewer than 256 such launches may be in flight
- *     at once on a device), and the 64 MiB array of pda_decode_step_noalloc.  The first launch
- *     of the head-group kernel on a device looks up its counters' address; make it before any
- *     stream capture, and make no launch on a device after cudaDeviceReset in the same process.
+ *     loads the library, two static arrays: 256 slots of per-launch counters, used by the fp8
+ *     head-group kernel and by the fused step's grid barrier (each such launch takes the next
+ *     slot; the launch's last CTA returns it to zero, so a captured launch can be replayed;
+ *     fewer than 256 such launches may be in flight at once on a device), and the 64 MiB array
+ *     of pda_decode_step_noalloc.  The first such launch on a device looks up the slots'
+ *     address; make it before any stream capture, and make no launch on a device after
+ *     cudaDeviceReset in the same process.
  *   - Launches are asynchronous on the caller's stream (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream).  Calls that share output or workspace buffers race
  *     if they overlap on the GPU.
@@ -212,21 +213,23 @@ PDA_API int pda_append_kv(const pda_plan_t* plan, const void* k_new, const void*
                           void* stream);
 
 /*
- * pda_decode_fused -- one launch for the whole step: the partition pass of pda_decode, and the
- * reduce of pda_reduce performed inside the same launch by the last partition of each
- * (sequence, KV head) to finish (the split-reduce pattern of "last arrival sums in order";
- * nothing waits).  A (sequence, KV head) whose context fits one partition is written to `out`
- * directly (its partial is not stored); the rows of a sequence with no tokens (context 0, or an
+ * pda_decode_fused -- one launch for the whole step: the partition pass of pda_decode, then, in
+ * the same launch, the reduce of pda_reduce.  The launch is cooperative (every CTA resident): once
+ * every CTA has written its partials they meet at a grid barrier (a bounded wait on a counter of
+ * the library's per-launch slots; a wait that gives up sets PDA_ERRW_PIPELINE_TIMEOUT), and then
+ * all of them merge the output rows, each row in partition order with pda_reduce's arithmetic, so
+ * results are deterministic and equal pda_decode + pda_reduce's bit for bit.  On head-warp plans a
+ * (sequence, KV head) whose context fits one partition is written to `out` by its partition's
+ * epilogue (its partial is not stored).  The rows of a sequence with no tokens (context 0, or an
  * invalid length, which also sets PDA_ERRW_BAD_CONTEXT_LEN) are written as zeros, as pda_reduce
- * writes them.  The combination is the one pda_reduce computes, in
- * partition order, so results are deterministic and equal pda_decode + pda_reduce's.
+ * writes them.
  *   partial_out, exp_sums, max_logits   as for pda_decode (scratch here)
- *   counters   device int32 [B][Hk]: must be zero before the first call; every completed call
- *              leaves them zero.  After a call that set PDA_ERRW_PIPELINE_TIMEOUT, zero them
- *              again before the next call.
+ *   counters   device int32 [B][Hk], zero: reserved (an earlier form of this step counted arrivals
+ *              there); the call leaves them zero.
  *   out, out_dtype                      as for pda_reduce
  * query, block_table, context_lens and out may be pinned host memory, as for pda_decode.
- * Calls that share counters or partials race if they overlap on the GPU.
+ * Calls that share partials race if they overlap on the GPU; fewer than 256 launches of this
+ * library's counter-slot kernels may be in flight on a device at once.
  * A TQ4 plan is rejected (PDA_ERR_INVALID_ARG): that format is read by pda_decode_tq4 only.
  */
 PDA_API int pda_decode_fused(const pda_plan_t* plan, const void* query, const void* kv_cache,

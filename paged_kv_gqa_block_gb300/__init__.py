@@ -248,7 +248,7 @@ def append_kv(p: Plan, k_new, v_new, kv_cache, num_cache_blocks: int, block_tabl
 
 
 def counters(p: Plan, device):
-    """Arrival counters of the fused step, int32 [B][Hk], zeroed (every completed step leaves them zero)."""
+    """The fused step's reserved counters argument, int32 [B][Hk], zeroed (the step leaves them zero)."""
     return torch.zeros((p.num_seqs, p.num_kv_heads), dtype=torch.int32, device=device)
 
 

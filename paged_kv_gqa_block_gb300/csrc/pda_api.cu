@@ -243,8 +243,8 @@ static bool use_head_groups(const pda_plan_t* plan) {
     return units >= 2ll * 2 * device_sm_count();
 }
 
-// The partition pass; with `fused`, the same launch also combines each (sequence, KV head)'s
-// partials into `out` (last-arriving partition merges, counters re-armed to zero).
+// The partition pass; with `fused`, the same (cooperative) launch also combines the partials
+// into `out` after a grid barrier (`counters` is reserved and left untouched).
 static int decode_launch(const pda_plan_t* plan, const void* query, const void* kv_cache, long long num_cache_blocks,
                          const int* block_table, const int* context_lens, float* partial_out, float* exp_sums,
                          float* max_logits, int* err_word, void* stream, bool fused, int* counters, void* out,

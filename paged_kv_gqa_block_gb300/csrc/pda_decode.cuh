@@ -43,6 +43,7 @@
 #include "pda.h"
 #include "pda_internal.h"
 #include "pda_ptx.cuh"
+#include "pda_merge.cuh"
 
 namespace pda {
 
@@ -875,118 +876,59 @@ struct Decode {
             *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow * kHeadDim + (lane << 2)) = u;
         }
     }
-    // The partitions' partials of one (sequence, head), combined in partition order exactly as the
-    // reduce kernel combines them: M = max m_p, w_p = l_p e^(m_p - M), out = sum (w_p / sum w) o_p.
-    // Up to 64 partitions: one round of loads brings (m_p, l_p) of every row, weights and sums
-    // stay in registers, and each row's partials are read sixteen at a time.
-    static __device__ void merge_unit(const DecodeArgs& a, const UnitIt& u, int lane) {
-        constexpr int QR = NT * 8;
-        const int nv = u.nv;
-        const long long base = (long long)(u.b * a.Hk + u.h) * a.P * a.QG;   // (p = 0, q = 0)
-        const long long orow0 = (long long)u.b * a.Hk * a.QG + (long long)u.h * a.QG;
-        const long long pstride = (long long)a.QG * kHeadDim;
-        if (nv > 64) {
-            merge_unit_general(a, u, lane);
-            return;
+    // The fused step's reduce, after the partition pass of every CTA: a grid barrier (the launch is
+    // cooperative, so every CTA is resident and the bounded wait ends), then the CTAs (one warp
+    // each) take the output rows round robin and merge each with merge_row, the arithmetic of the
+    // reduce kernel (same bits as pda_decode + pda_reduce).  A row of a single-partition unit was
+    // written by that unit's epilogue; a row of a sequence without tokens is written as zeros.
+    // The launch's counter slot {arrived, left} is zero at launch; its last CTA to leave resets it.
+    static __device__ __noinline__ void finish_fused(const DecodeArgs& a, int lane, bool ok) {
+        unsigned int* const bar = a.sched;
+        const bool alone = gridDim.x == 1;   // one CTA: it waits for no one and counts nothing
+        if (!alone) __threadfence();         // this CTA's partials and statistics, before it is counted
+        __syncwarp();
+        int arrived = alone ? 1 : 0;
+        if (lane == 0 && !alone) {
+            atomicAdd(bar, 1u);
+            const uint64_t t0 = global_timer_ns();
+            unsigned int backoff = 32;
+            while ((arrived = ld_acquire_gpu(reinterpret_cast<const int*>(bar))) < (int)gridDim.x) {
+                if (global_timer_ns() - t0 > a.timeout_ns) break;
+                __nanosleep(backoff);
+                backoff = min(backoff * 2, 256u);
+            }
         }
-        float coef[2][QR];
-        {
-            float mv[2][QR], lv[2][QR];
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int p = lane + 32 * c;
-#pragma unroll
-                for (int q = 0; q < QR; ++q) {
-                    const bool ok = p < nv && q < a.QG;
-                    mv[c][q] = ok ? __ldcg(a.max_logits + base + (long long)p * a.QG + q) : -INFINITY;
-                    lv[c][q] = ok ? __ldcg(a.exp_sums + base + (long long)p * a.QG + q) : 0.f;
+        arrived = __shfl_sync(kFull, arrived, 0);
+        if (arrived < (int)gridDim.x) {
+            ok = false;
+        } else {
+            const MergeArgs mg{a.partial_out, a.exp_sums, a.max_logits, a.out, a.Hk, a.QG, a.P, a.W, a.out_f32};
+            const int max_ctx = a.MB * a.BS;
+            const long long rows = (long long)a.B * a.Hk * a.QG, rps = (long long)a.Hk * a.QG;
+            int cb = -1, c = 0;   // the last sequence whose context length was read, and that length
+            for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+                const int b = (int)(row / rps);
+                const int rem = (int)(row - (long long)b * rps);
+                const int h = rem / a.QG, q = rem - h * a.QG;
+                if (b != cb) {
+                    cb = b;
+                    c = sanitize_ctx(__ldcg(a.context_lens + b), max_ctx);
+                }
+                if ((c + a.W - 1) / a.W == 1) continue;   // written by the unit's epilogue
+                merge_row(mg, b, h, q, c);
+            }
+        }
+        if (lane == 0) {
+            if (!ok && a.err_word) atomicOr(a.err_word, PDA_ERRW_PIPELINE_TIMEOUT);
+            if (!alone) {
+                __threadfence();
+                if (atomicAdd(bar + 1, 1u) == gridDim.x - 1) {   // every CTA has left the barrier
+                    bar[0] = 0u;
+                    bar[1] = 0u;
                 }
             }
-#pragma unroll
-            for (int q = 0; q < QR; ++q) {
-                float M = fmaxf(mv[0][q], mv[1][q]);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-                const float w0 = partition_weight(lv[0][q], mv[0][q], M);
-                const float w1 = partition_weight(lv[1][q], mv[1][q], M);
-                float wsum = __fadd_rn(w0, w1);   // the reduce kernel's order: chunk 0 then chunk 1
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) wsum = __fadd_rn(wsum, __shfl_xor_sync(kFull, wsum, o));
-                coef[0][q] = __fdiv_rn(w0, wsum);
-                coef[1][q] = __fdiv_rn(w1, wsum);
-            }
         }
-#pragma unroll
-        for (int q = 0; q < QR; ++q) {
-            if (q >= a.QG) break;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float* op = a.partial_out + (base + q) * kHeadDim + (lane << 2);
-            for (int p0 = 0; p0 < nv; p0 += 16) {
-                float4 o[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j)   // clamped index: every load is in bounds, extras weigh 0
-                    o[j] = __ldcg(reinterpret_cast<const float4*>(op + (long long)min(p0 + j, nv - 1) * pstride));
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int p = p0 + j;
-                    const float cf = __shfl_sync(kFull, (p & 32) ? coef[1][q] : coef[0][q], p & 31);
-                    if (p < nv) {
-                        acc.x = fmaf(cf, o[j].x, acc.x);
-                        acc.y = fmaf(cf, o[j].y, acc.y);
-                        acc.z = fmaf(cf, o[j].z, acc.z);
-                        acc.w = fmaf(cf, o[j].w, acc.w);
-                    }
-                }
-            }
-            store_out(a, orow0 + q, lane, acc);
-        }
-    }
-    // Any number of partitions, one row at a time.
-    static __device__ __noinline__ void merge_unit_general(const DecodeArgs& a, const UnitIt& u, int lane) {
-        const int nv = u.nv;
-        const long long base = (long long)(u.b * a.Hk + u.h) * a.P * a.QG;
-        const long long orow0 = (long long)u.b * a.Hk * a.QG + (long long)u.h * a.QG;
-        const long long pstride = (long long)a.QG * kHeadDim;
-        for (int q = 0; q < a.QG; ++q) {
-            float M = -INFINITY;
-            for (int p = lane; p < nv; p += 32) M = fmaxf(M, __ldcg(a.max_logits + base + (long long)p * a.QG + q));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-            float wsum = 0.f;
-            for (int p = lane; p < nv; p += 32) {
-                const long long i = base + (long long)p * a.QG + q;
-                wsum = __fadd_rn(wsum, partition_weight(__ldcg(a.exp_sums + i), __ldcg(a.max_logits + i), M));
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) wsum = __fadd_rn(wsum, __shfl_xor_sync(kFull, wsum, o));
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float* op = a.partial_out + (base + q) * kHeadDim + (lane << 2);
-            for (int p = 0; p < nv; ++p) {
-                float coef = 0.f;
-                if (lane == (p & 31)) {
-                    const long long i = base + (long long)p * a.QG + q;
-                    coef = __fdiv_rn(partition_weight(__ldcg(a.exp_sums + i), __ldcg(a.max_logits + i), M), wsum);
-                }
-                const float cf = __shfl_sync(kFull, coef, p & 31);
-                const float4 o = __ldcg(reinterpret_cast<const float4*>(op + (long long)p * pstride));
-                acc.x = fmaf(cf, o.x, acc.x);
-                acc.y = fmaf(cf, o.y, acc.y);
-                acc.z = fmaf(cf, o.z, acc.z);
-                acc.w = fmaf(cf, o.w, acc.w);
-            }
-            store_out(a, orow0 + q, lane, acc);
-        }
-    }
-
-    // The fused step writes every output row.  A sequence with no tokens (context 0, or an invalid
-    // length, read as 0) has no unit, so its rows are zeroed here, as the reduce would; sequence b
-    // falls to CTA b mod grid.  Its context length was just read by find_range (L1-resident).
-    static __device__ void zero_empty_outputs(const DecodeArgs& a, int lane) {
-        const long long rows = (long long)a.Hk * a.QG;
-        for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
-            if (sanitize_ctx(__ldg(a.context_lens + b), a.MB * a.BS) != 0) continue;
-            for (long long r = 0; r < rows; ++r) store_out(a, (long long)b * rows + r, lane, make_float4(0.f, 0.f, 0.f, 0.f));
-        }
+        __syncwarp();
     }
 
     // ------------------------------------------------------------------ the warp
@@ -1008,8 +950,10 @@ struct Decode {
         UnitIt cu;
         long long hi;
         find_range(a, cu, hi);
-        if constexpr (FUSED) zero_empty_outputs(a, lane);
-        if (!(cu.b < a.B && cu.start < hi)) return;
+        if (!(cu.b < a.B && cu.start < hi)) {
+            if constexpr (FUSED) finish_fused(a, lane, true);
+            return;
+        }
 
         // Q rows and the first block-table entries are requested before anything waits
         uint32_t qn[NT][16];
@@ -1286,21 +1230,6 @@ struct Decode {
             // the staging stage goes back to the feed (its generic writes precede the copy)
             fence_proxy_async_shared();
             if (feed_one(a, hi, kv_map, sc_map, sbase, bar0 + 8 * stage, stage, f, lane)) ++issued;
-            if constexpr (FUSED) {
-                if (cu.nv > 1) {
-                    // publish this partial; the last partition of the (sequence, head) to arrive merges all
-                    __threadfence();
-                    __syncwarp();
-                    int old = 0;
-                    if (lane == 0) old = atomicAdd(a.counters + (long long)cu.b * a.Hk + cu.h, 1);
-                    old = __shfl_sync(kFull, old, 0);
-                    if (old == cu.nv - 1) {
-                        __threadfence();
-                        merge_unit(a, cu, lane);
-                        if (lane == 0) a.counters[(long long)cu.b * a.Hk + cu.h] = 0;   // re-armed for the next step
-                    }
-                }
-            }
             if (!has_next) break;
             cu = nx;
         }
@@ -1317,6 +1246,7 @@ struct Decode {
             }
             __syncwarp();
         }
+        if constexpr (FUSED) finish_fused(a, lane, ok);
     }
 };
 

@@ -23,16 +23,17 @@ int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUte
     return launch_partition<PDA_KV_FP8_E4M3, 2, 4, 8, false>(a, kv_map, sc_map, stream);
 }
 
-// Counters of the head-group kernel: kSchedSlots slots of kSchedInts counters ({next unit,
-// producers done} for the partition pass; {next unit, -, -, -, CTAs done} for the fused step),
-// every slot zero between launches (each launch's last CTA returns its slot to zero).  Each launch takes the next slot in turn, so launches in flight at the same time (on
-// other streams) use different slots as long as fewer than kSchedSlots of them overlap.  The array
-// lives in every GPU that loads the library.
+// Per-launch counters: kSchedSlots slots of kSchedInts counters ({next unit, producers done} for
+// the head-group partition pass; {next unit, -, -, -, CTAs done} for its fused step; {arrived,
+// left} for the grid barrier of the head-warp fused step), every slot zero between launches (each
+// launch's last CTA returns its slot to zero).  Each launch takes the next slot in turn, so
+// launches in flight at the same time (on other streams) use different slots as long as fewer than
+// kSchedSlots of them overlap.  The array lives in every GPU that loads the library.
 constexpr int kSchedSlots = 256, kSchedInts = 8;
 static __device__ unsigned int g_group_sched[kSchedInts * kSchedSlots];
 
-// Device address of this launch's pair (the array's address is looked up once per device).
-static unsigned int* group_sched_slot(int* status) {
+// Device address of this launch's slot (the array's address is looked up once per device).
+unsigned int* launch_counter_slot(int* status) {
     static unsigned int* base[64] = {nullptr};
     static std::mutex mu;
     static std::atomic<unsigned long long> seq{0};
@@ -72,7 +73,7 @@ static int launch_groups(const DecodeArgs& a, const CUtensorMap& kv_map, const C
     static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PDA_ERR_CUDA;
-    const int threads = 32 * (a.HG + (FUSED ? 2 : 1));   // producer, HG consumers (, merger)
+    const int threads = 32 * (a.HG + 1);   // producer, HG consumers
     const int smem = group_smem_bytes(a.HG, S);
     if (a.HG < 1 || threads > 32 * NWARPS) return PDA_ERR_INVALID_ARG;
     int occ;
@@ -93,7 +94,7 @@ static int launch_groups(const DecodeArgs& a, const CUtensorMap& kv_map, const C
     if (sms <= 0) return PDA_ERR_CUDA;
     int rc = PDA_OK;
     DecodeArgs ag = a;
-    ag.sched = group_sched_slot(&rc);
+    ag.sched = launch_counter_slot(&rc);
     if (rc != PDA_OK) return rc;
     const long long units = (long long)a.B * (a.Hk / a.HG) * a.P;
     long long grid = (long long)sms * occ;
@@ -104,22 +105,27 @@ static int launch_groups(const DecodeArgs& a, const CUtensorMap& kv_map, const C
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (FUSED) {   // the fused step ends with a grid barrier: every CTA must be resident
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, kernel, kv_map, sc_map, ag) == cudaSuccess ? PDA_OK : PDA_ERR_LAUNCH;
 }
 
 int launch_decode_fp8_groups(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
                              bool fused, cudaStream_t stream) {
-    // up to 4 heads a CTA: two CTAs of up to 5 warps (6 for the fused step) per SM, each with 6
+    // up to 4 heads a CTA: two CTAs of up to 5 warps per SM, each with 6
     // stages of up to 17 KB (two independent producers per SM, whose consumers reach their unit
     // boundaries at different times, measured faster than one CTA of 8 heads with 6 stages of 33 KB)
     if (fused) {
-        if (a.QG <= 8) return launch_groups<1, 6, 6, 2, true>(a, kv_map, sc_map, stream);
-        return launch_groups<2, 6, 6, 2, true>(a, kv_map, sc_map, stream);
+        if (a.QG <= 8) return launch_groups<1, 6, 5, 2, true>(a, kv_map, sc_map, stream);
+        return launch_groups<2, 6, 5, 2, true>(a, kv_map, sc_map, stream);
     }
     if (a.QG <= 8) return launch_groups<1, 6, 5, 2, false>(a, kv_map, sc_map, stream);
     return launch_groups<2, 6, 5, 2, false>(a, kv_map, sc_map, stream);

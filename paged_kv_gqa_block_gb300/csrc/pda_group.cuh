@@ -396,8 +396,6 @@ struct GroupDecode {
         }
         int cs = 0;
         uint32_t cph = 0;
-        GroupUnit done;   // fused step: the last unit whose partial this consumer wrote and has not yet reported
-        done.valid = false;
         for (long long i = 0; u.valid && ok; ++i) {
             const int h = u.g * HG + c;
             // ---- Q fragments: every bf16 bit of Q kept in f16 by a power-of-two scale
@@ -426,16 +424,12 @@ struct GroupDecode {
                         qf[n][kk][1] = pack_f16(bf16_lo(y) * pw, bf16_hi(y) * pw);
                     }
             }
-            // ---- the next unit's Q rows are requested while this unit runs: right away, or, in the
-            // fused step, after the previous unit's partial has been reported (the report's fence
-            // would otherwise wait for these loads)
+            // ---- the next unit's Q rows are requested while this unit runs
             const GroupUnit nx = read_unit(m, i + 1, lane, ok, a.timeout_ns);
             if (!ok) break;
-            bool q_pending = nx.valid;
-            if (q_pending && !(FUSED && done.valid)) {
+            if (nx.valid) {
                 UnitIt ui{nx.b, nx.g * HG + c, nx.p, nx.ctx, 0, 0};
                 D::load_q(a, ui, qn, lane);
-                q_pending = false;
             }
 
             float acc[NT][8][4];
@@ -478,15 +472,6 @@ struct GroupDecode {
                         reinterpret_cast<const float*>(m.ptr + m.off_scales + s0 * scale_bytes + c * 128)};
                     const int vv[1] = {v0};
                     D::template step_fp8<1>(st, sc, vv, cq, qf, acc, m2, mt, ls, F, rF, lane);
-                }
-                if (FUSED && done.valid) {   // the previous unit's bulk copy has long completed by now
-                    report_done(a, done, lane);
-                    done.valid = false;
-                }
-                if (q_pending) {
-                    UnitIt ui{nx.b, nx.g * HG + c, nx.p, nx.ctx, 0, 0};
-                    D::load_q(a, ui, qn, lane);
-                    q_pending = false;
                 }
                 t += two ? 2 : 1;
                 // the stages go back to the producer once every lane's reads of them are done; the
@@ -577,10 +562,8 @@ struct GroupDecode {
                         }
                     }
             }
-            if constexpr (FUSED) done = u;
             u = nx;
         }
-        if (FUSED && done.valid && ok) report_done(a, done, lane);
         if (lane == 0) {
             if (!ok && a.err_word) atomicOr(a.err_word, PDA_ERRW_PIPELINE_TIMEOUT);
             bulk_wait_all();   // the partials are written before the CTA retires
@@ -589,66 +572,28 @@ struct GroupDecode {
     }
 
     // ------------------------------------------------------------------ fused step
-    // Counters of the fused step (caller's `counters`, int32 [B][Hk], zero at launch and left zero):
-    // entry b*NG + g counts the partials of head group g of sequence b that are written (one per
-    // consumer per unit; complete at nv*HG).  The launch's counter slot holds {next unit, -, -, -,
-    // CTAs done}.
-
-    // This consumer's partial of unit u (and its statistics) is written: count it.
-    static __device__ void report_done(const DecodeArgs& a, const GroupUnit& u, int lane) {
-        if (lane == 0) {
-            bulk_wait_all();              // the bulk copy of the partial has completed ...
-            fence_proxy_async_global();   // ... and is ordered before what follows
-        }
-        __threadfence();                  // every lane's statistics stores, before the count
-        __syncwarp();
-        if (lane == 0) atomicAdd(a.counters + (long long)u.b * (a.Hk / a.HG) + u.g, 1);
-        __syncwarp();
-    }
-
-    // Merges this warp's share of the output rows (b, h, q), in row order.  Rows of long sequences
-    // (complete early, while the pass still streams) go to the CTAs' merger warps, dealt round robin;
-    // the other rows (complete near the end) to every warp of the launch.  A row waits (bounded)
-    // until every partial of its head group is counted: only CTAs already running hold units, so
-    // the wait ends.  Rows of sequences without tokens are written as zeros.
-    static __device__ void merge_rows(const DecodeArgs& a, bool merger, int lane, bool& ok) {
-        const int max_ctx = a.MB * a.BS, NG = a.Hk / a.HG, nwarps = blockDim.x >> 5;
-        const long long rows = (long long)a.B * a.Hk * a.QG;
-        const long long mstride = gridDim.x, mfirst = blockIdx.x;                       // merger warps
-        const long long astride = (long long)gridDim.x * nwarps,
-                        afirst = (long long)blockIdx.x * nwarps + (threadIdx.x >> 5);  // every warp
+    // After every CTA's partition pass (a grid barrier: the launch is cooperative, so every CTA is
+    // resident and the bounded wait ends), every warp of the launch merges its share of the output
+    // rows, dealt round robin, with merge_row (the reduce kernel's arithmetic: the same bits as
+    // pda_decode + pda_reduce).  Rows of sequences without tokens are written as zeros.  The
+    // launch's counter slot holds {next unit, -, -, -, CTAs done, CTAs arrived}.
+    static __device__ __noinline__ void merge_all(const DecodeArgs& a, int lane) {
+        const int max_ctx = a.MB * a.BS, nwarps = blockDim.x >> 5;
+        const long long rows = (long long)a.B * a.Hk * a.QG, rps = (long long)a.Hk * a.QG;
         const MergeArgs mg{a.partial_out, a.exp_sums, a.max_logits, a.out, a.Hk, a.QG, a.P, a.W, a.out_f32};
-        for (int pass = 0; pass < 2 && ok; ++pass) {
-            if (pass == 0 && !merger) continue;
-            const long long first = pass == 0 ? mfirst : afirst, stride = pass == 0 ? mstride : astride;
-            for (long long row = first; row < rows && ok; row += stride) {
-                const long long unit = row / a.QG;
-                const int q = (int)(row - unit * a.QG);
-                const int b = (int)(unit / a.Hk), h = (int)(unit - (long long)b * a.Hk);
-                const int c = sanitize_ctx(__ldg(a.context_lens + b), max_ctx);
-                if (group_long(c, a.W) != (pass == 0)) continue;
-                const int nv = group_nv(c, a.W);
-                if (nv > 0) {
-                    int seen = 0;
-                    if (lane == 0) {
-                        const int* cnt = a.counters + (long long)b * NG + h / a.HG;
-                        const uint64_t t0 = global_timer_ns();
-                        unsigned int backoff = 64;
-                        while ((seen = ld_acquire_gpu(cnt)) < nv * a.HG) {
-                            if (global_timer_ns() - t0 > a.timeout_ns) break;
-                            __nanosleep(backoff);
-                            backoff = min(backoff * 2, 1024u);
-                        }
-                    }
-                    seen = __shfl_sync(kFull, seen, 0);
-                    if (seen < nv * a.HG) {
-                        ok = false;
-                        break;
-                    }
-                }
-                merge_row(mg, b, h, q, c);
+        int cb = -1, c = 0;   // the last sequence whose context length was read, and that length
+        for (long long row = (long long)blockIdx.x * nwarps + (threadIdx.x >> 5); row < rows;
+             row += (long long)gridDim.x * nwarps) {
+            const int b = (int)(row / rps);
+            const int rem = (int)(row - (long long)b * rps);
+            const int h = rem / a.QG, q = rem - h * a.QG;
+            if (b != cb) {
+                cb = b;
+                c = sanitize_ctx(__ldcg(a.context_lens + b), max_ctx);
             }
+            merge_row(mg, b, h, q, c);
         }
+        (void)lane;
     }
     static __device__ void run(const DecodeArgs& a, const CUtensorMap* kv_map, const CUtensorMap* sc_map,
                                uint8_t* smem) {
@@ -690,32 +635,43 @@ struct GroupDecode {
             else if (warp <= HG)
                 consume(a, warp - 1, m);
         } else {
-            // producer, consumers, and one warp that merges from the start; the others merge their
-            // share of the rows once they have no unit left
             if (warp == 0)
                 produce(a, kv_map, sc_map, m);
             else if (warp <= HG)
                 consume(a, warp - 1, m);
-            bool ok = true;
-            merge_rows(a, warp == HG + 1, lane, ok);
-            if (!ok && lane == 0 && a.err_word) atomicOr(a.err_word, PDA_ERRW_PIPELINE_TIMEOUT);
-            // the launch's last CTA returns the counters to zero
+            // the CTA's partials are written (each consumer waited for its bulk copies): order them,
+            // and the statistics, before the CTA is counted
+            if (warp >= 1 && warp <= HG && lane == 0) fence_proxy_async_global();
+            __threadfence();
             __syncthreads();
-            if (warp == 0) {
+            __shared__ int arrived_all;
+            const bool alone = gridDim.x == 1;   // one CTA: it waits for no one
+            if (threadIdx.x == 0 && alone) arrived_all = 1;
+            if (threadIdx.x == 0 && !alone) {
+                atomicAdd(a.sched + 5, 1u);
+                const uint64_t t0 = global_timer_ns();
+                unsigned int backoff = 32;
+                int arrived = 0;
+                while ((arrived = ld_acquire_gpu(reinterpret_cast<const int*>(a.sched + 5))) < (int)gridDim.x) {
+                    if (global_timer_ns() - t0 > a.timeout_ns) break;
+                    __nanosleep(backoff);
+                    backoff = min(backoff * 2, 256u);
+                }
+                arrived_all = arrived >= (int)gridDim.x;
+            }
+            __syncthreads();
+            if (arrived_all)
+                merge_all(a, lane);
+            else if (threadIdx.x == 0 && a.err_word)
+                atomicOr(a.err_word, PDA_ERRW_PIPELINE_TIMEOUT);
+            // the launch's last CTA returns the slot to zero
+            __syncthreads();
+            if (threadIdx.x == 0) {
                 __threadfence();
-                unsigned int old = 0;
-                if (lane == 0) old = atomicAdd(a.sched + 4, 1u);
-                old = __shfl_sync(kFull, old, 0);
-                if (old == gridDim.x - 1) {
+                if (atomicAdd(a.sched + 4, 1u) == gridDim.x - 1) {   // (also resets the unit counter)
+                    a.sched[0] = a.sched[1] = a.sched[2] = a.sched[3] = a.sched[5] = 0u;
                     __threadfence();
-                    const long long groups = (long long)a.B * (a.Hk / a.HG);
-                    for (long long i = lane; i < groups; i += 32) a.counters[i] = 0;
-                    __syncwarp();
-                    if (lane == 0) {
-                        a.sched[0] = a.sched[1] = a.sched[2] = a.sched[3] = 0u;
-                        __threadfence();
-                        a.sched[4] = 0u;
-                    }
+                    a.sched[4] = 0u;
                 }
             }
         }

@@ -26,12 +26,12 @@ struct DecodeArgs {
     int B, Hk, QG, MB, BS, P, W;
     int bs_shift;              // log2(BS)
     int HG;                    // head-group kernel: KV heads per CTA (a divisor of Hk, <= 4)
-    unsigned int* sched;       // head-group kernel: this launch's slot of counters, zero at launch
-                               // and left zero by the launch's last CTA (or warp, fused step)
+    unsigned int* sched;       // this launch's slot of counters (head-group kernel; the fused step's
+                               // grid barrier), zero at launch and left zero by its last CTA
     float qk_scale_log2;       // softmax_scale * log2(e)
     unsigned long long timeout_ns;
-    // fused step only: per-(sequence, KV head) arrival counters and the final output
-    int* counters;             // [B][Hk], zero before the launch, left zero after it
+    // fused step only: the caller's reserved counters (untouched) and the final output
+    int* counters;             // [B][Hk], zero
     void* out;                 // [B][Hk*QG][D] bf16 or fp32
     int out_f32;
 };
@@ -52,14 +52,18 @@ int launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& kv_map, bool fuse
 int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, bool fused,
                       cudaStream_t stream);
 // The head-group kernel (fp8): a.HG heads per CTA; the maps' boxes span a.HG heads.
-// With `fused`, the same launch also combines the partials into `out` (a.counters as the fused
-// step's counters).
+// With `fused`, the same (cooperative) launch also combines the partials into `out` after a
+// grid barrier.
 int launch_decode_fp8_groups(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
                              bool fused, cudaStream_t stream);
 // KV heads per CTA of the head-group kernel for Hk heads: the largest divisor of Hk not above 4.
 int group_heads(int Hk);
 int launch_decode_tq4(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, cudaStream_t stream);
 int launch_reduce(const ReduceArgs& r, cudaStream_t stream);
+
+// The next slot of per-launch counters on the current device (zero; the launch's last CTA leaves
+// it zero).  Sets *status to a pda_status value.
+unsigned int* launch_counter_slot(int* status);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

@@ -39,19 +39,30 @@ int launch_partition(const DecodeArgs& a, const CUtensorMap& kv_map, const CUten
     long long grid = (long long)sms * occ;
     if (grid > units) grid = units;
     if (grid < 1) return PDA_OK;
-    // programmatic dependent launch: the prologue may overlap the tail of the previous grid; the
-    // kernel waits for that grid before it reads any input
+    DecodeArgs af = a;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(Cfg::kThreads);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    // programmatic dependent launch: the prologue may overlap the tail of the previous grid; the
+    // kernel waits for that grid before it reads any input
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, kv_map, sc_map, a) == cudaSuccess ? PDA_OK : PDA_ERR_LAUNCH;
+    if (FUSED) {
+        // the fused step ends with a grid barrier: a cooperative launch keeps every CTA resident
+        // (the grid is at most the resident CTAs), and the barrier counts in this launch's slot
+        int rc = PDA_OK;
+        af.sched = launch_counter_slot(&rc);
+        if (rc != PDA_OK) return rc;
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+        cfg.numAttrs = 2;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, kv_map, sc_map, af) == cudaSuccess ? PDA_OK : PDA_ERR_LAUNCH;
 }
 
 }  // namespace pda

@@ -117,14 +117,17 @@ def test_fused_full_size_equals_two_launch(pda, name, variant):
         assert np.array_equal(o, two)
 
 
-def test_fused_head_groups_counters_return_to_zero_across_many_launches(oracle_mod, pda):
-    # the fused head-group step takes a counter slot per launch (256 of them) and leaves its slot
-    # and the caller's counters at zero: 600 launches in a row give the first launch's bits
+@pytest.mark.parametrize("kv,variant", [(wl.KV_BF16, 0), (wl.KV_FP8_E4M3, 1), (wl.KV_FP8_E4M3, 2)])
+def test_fused_counters_return_to_zero_across_many_launches(oracle_mod, pda, kv, variant):
+    # the fused step takes a counter slot per launch (256 of them: the head-group scheduler's, or
+    # the head-warp step's grid barrier) and leaves its slot and the caller's counters at zero:
+    # 600 launches in a row give the first launch's bits (a slot left non-zero would let a later
+    # launch merge before its partials exist)
     w = wl.small(num_seqs=5, num_kv_heads=8, query_group_size=6, kv_block_size=16, ctx=(3000, 17, 0, 1200, 256),
-                 kv_dtype=wl.KV_FP8_E4M3, seed=97)
+                 kv_dtype=kv, seed=97)
     inp = wl.generate(w)
     d = to_device(inp)
-    p = plan_for(w, variant=2)
+    p = plan_for(w, variant=variant)
     ws = pda.workspace(p, "cuda")
     cnt = pda.counters(p, "cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -138,7 +141,45 @@ def test_fused_head_groups_counters_return_to_zero_across_many_launches(oracle_m
     torch.cuda.synchronize()
     assert int(err.item()) == 0 and int(cnt.abs().sum().item()) == 0
     assert torch.equal(first, last)
-    assert np.abs(first.cpu().numpy() - oh.run_oracle(inp)["out"]).max() <= TOL[wl.KV_FP8_E4M3]
+    assert np.abs(first.cpu().numpy() - oh.run_oracle(inp)["out"]).max() <= TOL[kv]
+
+
+@pytest.mark.parametrize("kv,variant", [(wl.KV_BF16, 0), (wl.KV_FP8_E4M3, 1), (wl.KV_FP8_E4M3, 2)])
+def test_fused_step_replays_in_a_cuda_graph(oracle_mod, pda, kv, variant):
+    # a captured fused step keeps the counter slot it took at capture: every replay finds it zero
+    # again (the launch's last CTA resets it) and reads the context lengths as they are then
+    w = wl.small(num_seqs=4, num_kv_heads=4, ctx=(700, 33, 256, 1500), kv_dtype=kv, seed=81, max_blocks_per_seq=100)
+    inp = wl.generate(w)
+    d = to_device(inp)
+    p = plan_for(w, variant=variant)
+    ws = pda.workspace(p, "cuda")
+    cnt = pda.counters(p, "cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty((w.num_seqs, w.num_q_heads, 128), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+
+    def step():
+        pda.decode_fused(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"],
+                         ws["partial_out"], ws["exp_sums"], ws["max_logits"], cnt, out, err_word=err)
+    with torch.cuda.stream(s):     # one direct call first: per-device set-up happens outside capture
+        step()
+    torch.cuda.synchronize()
+    direct = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, direct)
+    new_ctx = np.array([300, 1, 0, 1499], np.int32)
+    d["context_lens"].copy_(torch.from_numpy(new_ctx))
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and int(cnt.abs().sum().item()) == 0
+    ref = oh.run_oracle(wl.Inputs(w, inp.query, inp.cache, inp.block_table, new_ctx, inp.extra))["out"]
+    assert np.abs(out.cpu().numpy() - ref).max() <= TOL[kv]
 
 
 @pytest.mark.parametrize("kv,variant", [(wl.KV_BF16, 0), (wl.KV_FP8_E4M3, 1), (wl.KV_FP8_E4M3, 2)])
