@@ -577,7 +577,7 @@ struct GroupDecode {
     // rows, dealt round robin, with merge_row (the reduce kernel's arithmetic: the same bits as
     // pda_decode + pda_reduce).  Rows of sequences without tokens are written as zeros.  The
     // launch's counter slot holds {next unit, -, -, -, CTAs done, CTAs arrived}.
-    static __device__ __noinline__ void merge_all(const DecodeArgs& a, int lane) {
+    static __device__ __noinline__ void merge_all(const DecodeArgs& a) {
         const int max_ctx = a.MB * a.BS, nwarps = blockDim.x >> 5;
         const long long rows = (long long)a.B * a.Hk * a.QG, rps = (long long)a.Hk * a.QG;
         const MergeArgs mg{a.partial_out, a.exp_sums, a.max_logits, a.out, a.Hk, a.QG, a.P, a.W, a.out_f32};
@@ -593,7 +593,6 @@ struct GroupDecode {
             }
             merge_row(mg, b, h, q, c);
         }
-        (void)lane;
     }
     static __device__ void run(const DecodeArgs& a, const CUtensorMap* kv_map, const CUtensorMap* sc_map,
                                uint8_t* smem) {
@@ -661,7 +660,7 @@ struct GroupDecode {
             }
             __syncthreads();
             if (arrived_all)
-                merge_all(a, lane);
+                merge_all(a);
             else if (threadIdx.x == 0 && a.err_word)
                 atomicOr(a.err_word, PDA_ERRW_PIPELINE_TIMEOUT);
             // the launch's last CTA returns the slot to zero
