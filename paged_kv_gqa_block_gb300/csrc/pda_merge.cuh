@@ -1,5 +1,5 @@
 // pda_merge.cuh -- the combination of one query row's partition partials into its output row,
-// shared by the reduce kernel and the fused head-group step, so both give the same bits.
+// shared by the reduce kernel and the fused steps, so all give the same bits.
 //
 // For sequence b, KV head h and query row q with nv = ceil(ctx / W) partitions:
 //   M = max_p m_p,  w_p = l_p * e^(m_p - M),  out = sum_p (w_p / sum_p w_p) * o_p   (p < nv)
