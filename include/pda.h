@@ -22,10 +22,11 @@
  *     driver's tensor-map encoder and of per-device occupancy figures, and, in every GPU that
  *     loads the library, two static arrays: 256 slots of per-launch counters, used by the fp8
  *     head-group kernel and by the fused step's grid barrier (each such launch takes the next
- *     slot; the launch's last CTA returns it to zero, so a captured launch can be replayed;
- *     fewer than 256 such launches may be in flight at once on a device), and the 64 MiB array
- *     of pda_decode_step_noalloc.  The first such launch on a device looks up the slots'
- *     address; make it before any stream capture, and make no launch on a device after
+ *     slot in turn; the launch's last CTA returns it to zero, so a captured launch can be
+ *     replayed; two launches whose slots coincide, one taken 256 such launches after the other,
+ *     must not overlap on the GPU, and a graph replay keeps the slot taken at capture), and the
+ *     64 MiB array of pda_decode_step_noalloc.  The first such launch on a device looks up the
+ *     slots' address; make it before any stream capture, and make no launch on a device after
  *     cudaDeviceReset in the same process.
  *   - Launches are asynchronous on the caller's stream (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream).  Calls that share output or workspace buffers race
