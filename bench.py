@@ -45,6 +45,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
 L2_CLEAN_READ_BYTES = 256 << 20
+L2_BYTES = 129e6        # GB300 L2: a step whose KV reads exceed it gets no reuse from one step to the next
 # the files that make up the partition kernel (its ncu counters go stale when one changes)
 PARTITION_KERNEL_SOURCES = ("pda_decode.cuh", "pda_group.cuh", "pda_merge.cuh", "pda_ptx.cuh", "pda_launch.cuh",
                             "pda_internal.h", "pda_decode_bf16.cu", "pda_decode_fp8.cu", "pda_decode_tq4.cu",
@@ -359,6 +360,38 @@ def event_times(fn, n, flush, stream, before=None):
     return [a.elapsed_time(b) * 1e-3 for a, b in ev]
 
 
+def back_to_back_times(fn, n, stream, batches=10):
+    """Device time of n calls of `fn` issued back to back on `stream` (CUDA events around each of
+    `batches` equal batches, nothing between the calls); seconds per call, one figure per batch."""
+    import torch
+    if n % batches:   # exactly n calls: one batch unless n divides evenly
+        batches = 1
+    per = n // batches
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(batches)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        for _ in range(per):
+            fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e-3 / per for a, b in ev]
+
+
+def timing_mode(w, inp, W) -> str:
+    """How the steps are timed: back to back when the step's KV reads exceed L2 (no step then finds
+    the previous step's KV in L2), else each step alone after an L2 flush."""
+    return "back_to_back" if algorithmic_bytes(w, inp.context_lens, W)["kv"] > L2_BYTES else "flushed"
+
+
+def l2_note(mode, w, inp, W) -> str:
+    if mode == "back_to_back":
+        kv = algorithmic_bytes(w, inp.context_lens, W)["kv"]
+        return (f"inputs larger than L2: {kv / 1e6:.0f} MB of KV per step > {L2_BYTES / 1e6:.0f} MB L2; "
+                "steps timed back to back, no flush")
+    return "flushed between timed steps (512 MiB write, then 256 MiB read)"
+
+
 def rates(w, inp, p, mean_step, mean_dec, world, peak, peaks, kernel="pda_partition_kernel"):
     ab = algorithmic_bytes(w, inp.context_lens, p.partition_tokens)
     achieved = ab["decode"] / mean_dec / 1e9
@@ -400,9 +433,11 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     S = _Step(pda, w, inp, dev, stream, args.path, args.variant)
     step = S.step
+    mode = timing_mode(w, inp, S.p.partition_tokens)
 
     for _ in range(args.warmup):
-        flush()
+        if mode == "flushed":
+            flush()
         step()
     torch.cuda.synchronize()
     if args.graph:      # capture one step; the timed loops replay it
@@ -419,22 +454,32 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
     S.check_err()
 
-    # ---- device-resident timing: events around each whole step on the launching stream (nothing
-    # between the two launches, so the reduce can be scheduled while the partition pass drains)
+    # ---- device-resident timing on the launching stream (nothing between the two launches of a
+    # step, so the reduce can be scheduled while the partition pass drains): the K steps back to
+    # back when the step's KV exceeds L2, else events around each step after an L2 flush
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
         wall0 = time.perf_counter()
-        t_step = event_times(step, args.steps, flush, stream)
+        if mode == "back_to_back":
+            t_step = back_to_back_times(step, args.steps, stream)
+        else:
+            t_step = event_times(step, args.steps, flush, stream)
         wall = time.perf_counter() - wall0
     if dist:
         dist.barrier()
-    # the partition kernel alone (roofline of the dominant kernel)
+    # the partition kernel alone (roofline of the dominant kernel): each launch after an L2 flush,
+    # so its duration includes the cold start of every launch
     dec_steps = max(20, min(args.steps, 500))
     t_dec = event_times(S.decode, dec_steps, flush, stream)
     mean_step, mean_dec = sum(t_step) / len(t_step), sum(t_dec) / len(t_dec)
     med_step, min_step = float(np.median(t_step)), min(t_step)
+    flushed = None
+    if mode == "back_to_back":   # the same step alone after an L2 flush, for comparison
+        t_fl = event_times(step, max(20, min(args.steps, 500)), flush, stream)
+        flushed = {"ms_per_step": sum(t_fl) / len(t_fl) * 1e3, "step_ms_median": float(np.median(t_fl)) * 1e3,
+                   "how": "each step alone between CUDA events, L2 flushed before it"}
     if dist:
         mean_step, mean_dec = max_over_ranks(dist, [mean_step, mean_dec], dev)
 
@@ -444,29 +489,32 @@ def run_ours(args, rank, world, local_rank):
     # with one explicit copy of the packed inputs in and one of the output out.  The KV cache is
     # device-resident state in both.
     e2e_steps = max(10, min(args.steps, 500))
-    e2e = []
-    for i in range(e2e_steps + 3):
-        flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+
+    def step_with_copies():
         S.step_in.copy_(S.step_in_host, non_blocking=True)
         step()
         S.outh.copy_(S.out, non_blocking=True)
-        b.record(stream)
-        b.synchronize()
-        if i >= 3:
-            e2e.append(a.elapsed_time(b) * 1e-3)
-    mean_e2e = sum(e2e) / len(e2e)
-    e2e_zc = []
-    for i in range(e2e_steps + 3):
-        flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+
+    def step_on_host():
         S.step_on(S.qh, S.bth, S.ctxh, S.outh)
-        b.record(stream)
-        b.synchronize()
-        if i >= 3:
-            e2e_zc.append(a.elapsed_time(b) * 1e-3)
+    e2e, e2e_zc = [], []
+    if mode == "back_to_back":
+        for fn, acc in ((step_with_copies, e2e), (step_on_host, e2e_zc)):
+            for _ in range(3):
+                fn()
+            acc.extend(back_to_back_times(fn, e2e_steps, stream))
+    else:
+        for fn, acc in ((step_with_copies, e2e), (step_on_host, e2e_zc)):
+            for i in range(e2e_steps + 3):
+                flush()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                b.synchronize()
+                if i >= 3:
+                    acc.append(a.elapsed_time(b) * 1e-3)
+    mean_e2e = sum(e2e) / len(e2e)
     mean_e2e_zc = sum(e2e_zc) / len(e2e_zc)
     if dist:
         mean_e2e, mean_e2e_zc = max_over_ranks(dist, [mean_e2e, mean_e2e_zc], dev)
@@ -478,8 +526,9 @@ def run_ours(args, rank, world, local_rank):
     p = S.p
     units = S.units
 
-    # ---- the other configurations, timed the same way in the same run (device-resident inputs,
-    # L2 flushed between steps); each is generated, timed and freed in turn
+    # ---- the other configurations, timed the same way in the same run (device-resident inputs;
+    # back to back when their KV exceeds L2, else L2 flushed between steps); each is generated,
+    # timed and freed in turn
     others = []
     if not args.no_other_workloads:
         del S
@@ -490,12 +539,17 @@ def run_ours(args, rank, world, local_rank):
             wo = wl.WORKLOADS[name]
             io = wl.generate(wo)
             So = _Step(pda, wo, io, dev, stream, "two")
+            mo = timing_mode(wo, io, So.p.partition_tokens)
             for _ in range(max(3, args.warmup)):
-                flush()
+                if mo == "flushed":
+                    flush()
                 So.step()
             torch.cuda.synchronize()
             So.check_err()
-            ts = event_times(So.step, n_other, flush, stream)
+            if mo == "back_to_back":
+                ts = back_to_back_times(So.step, n_other, stream)
+            else:
+                ts = event_times(So.step, n_other, flush, stream)
             td = event_times(So.decode, n_other, flush, stream)
             So.check_err()
             ms, md = sum(ts) / len(ts), sum(td) / len(td)
@@ -504,7 +558,8 @@ def run_ours(args, rank, world, local_rank):
             _, r = rates(wo, io, So.p, ms, md, world, peak, peaks, kernel_name(pda, So.p))
             others.append({"workload": name, "kv_dtype": KV_NAMES[wo.kv_dtype], "steps": n_other,
                            "value": replica_throughput(world, So.units, ms), "unit": UNIT,
-                           "ms_per_step": ms * 1e3, "step_ms_median": float(np.median(ts)) * 1e3, **r})
+                           "ms_per_step": ms * 1e3, "step_ms_median": float(np.median(ts)) * 1e3,
+                           "l2": l2_note(mo, wo, io, So.p.partition_tokens), **r})
             del So, io
             torch.cuda.empty_cache()
 
@@ -525,7 +580,7 @@ def run_ours(args, rank, world, local_rank):
                    "query_group_size": w.query_group_size, "kv_block_size": w.kv_block_size,
                    "tile_groups_per_partition": p.resolved_tile_groups, "num_partitions": p.num_partitions,
                    "context_tokens": ab["tokens"], "seq_len_max": int(inp.context_lens.max()),
-                   "parallelism": f"replicas{world}", "l2": "flushed between timed steps (512 MiB write, then 256 MiB read)"},
+                   "parallelism": f"replicas{world}", "l2": l2_note(mode, w, inp, p.partition_tokens)},
         "query_head_steps_per_s": replica_throughput(world, units * w.query_group_size, mean_step),
         **r,
         "e2e": {"value": replica_throughput(world, units, mean_e2e_zc), "unit": UNIT,
@@ -541,9 +596,12 @@ def run_ours(args, rank, world, local_rank):
         "step_path": ("pda_decode_fused (one launch)" if args.path == "fused" else "pda_decode + pda_reduce") +
                      (", replayed from a CUDA graph" if args.graph else ""),
         "decode_launches_timed_separately": dec_steps,
+        "decode_timing": "each partition-kernel launch alone between CUDA events, L2 flushed before it",
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
     }
+    if flushed:
+        res["flushed"] = flushed
     if others:
         res["other_workloads"] = others
     if not args.no_cpu_baseline and world >= 1:
