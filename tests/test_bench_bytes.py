@@ -27,3 +27,21 @@ def test_algorithmic_bytes_by_hand(kv):
     assert ab["decode"] == kv_bytes + q + table + lengths + partials
     assert ab["reduce"] == partials + out   # the reduce reads the partials and writes the output
     assert ab["tokens"] == 57 and ab["units"] == 4
+
+
+def test_timing_mode_follows_the_kv_bytes_against_l2():
+    # a step whose KV reads exceed L2 is timed back to back (no step finds the previous step's KV
+    # in L2); a smaller one step by step after an L2 flush; the line's config says which
+    expect = {"b1_hk1_qg8_bs16_ctx256": "flushed", "b8_hk8_qg8_bs16_ctx1-4096": "flushed",
+              "b4_hk8_qg8_bs32_ctx32768_g5p32": "back_to_back", "b32_hk4_qg16_bs32_ctx2048-8192_kbias": "back_to_back",
+              "b64_hk8_qg6_bs16_fp8_lognormal2048": "back_to_back", "b64_hk8_qg6_bs16_tq4_lognormal2048": "back_to_back"}
+    for name, mode in expect.items():
+        w = wl.WORKLOADS[name]
+        inp = wl.generate(w)
+        W = 256 * max(1, w.tile_groups_per_partition)
+        kv = bench.algorithmic_bytes(w, inp.context_lens, W)["kv"]
+        assert (kv > bench.L2_BYTES) == (mode == "back_to_back"), name
+        assert bench.timing_mode(w, inp, W) == mode, name
+        note = bench.l2_note(mode, w, inp, W)
+        assert ("back to back" in note) == (mode == "back_to_back")
+        assert note.startswith("flushed") == (mode == "flushed")
