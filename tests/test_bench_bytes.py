@@ -3,6 +3,8 @@
 Two sequences of 40 and 17 tokens, 2 KV heads, QG 8, 16-token blocks, 256-token partitions:
 57 tokens per head, one partition each, 3 + 2 block-table entries.
 """
+import types
+
 import numpy as np
 import pytest
 
@@ -37,7 +39,8 @@ def test_timing_mode_follows_the_kv_bytes_against_l2():
               "b64_hk8_qg6_bs16_fp8_lognormal2048": "back_to_back", "b64_hk8_qg6_bs16_tq4_lognormal2048": "back_to_back"}
     for name, mode in expect.items():
         w = wl.WORKLOADS[name]
-        inp = wl.generate(w)
+        # the workload's context lengths are the generator's first draw (no cache is built here)
+        inp = types.SimpleNamespace(context_lens=wl.draw_context_lens(w, np.random.Generator(np.random.PCG64(w.seed))))
         W = 256 * max(1, w.tile_groups_per_partition)
         kv = bench.algorithmic_bytes(w, inp.context_lens, W)["kv"]
         assert (kv > bench.L2_BYTES) == (mode == "back_to_back"), name
