@@ -232,6 +232,9 @@ PDA_API int pda_append_kv(const pda_plan_t* plan, const void* k_new, const void*
  * Calls that share partials race if they overlap on the GPU; fewer than 256 launches of this
  * library's counter-slot kernels may be in flight on a device at once.
  * A TQ4 plan is rejected (PDA_ERR_INVALID_ARG): that format is read by pda_decode_tq4 only.
+ * On GB300 this step measured slower than pda_decode followed by pda_reduce on every workload
+ * timed (the reduce launch is already resident when the partition pass ends; the barrier and
+ * the merge after it cost more); it exists for callers that want a single launch.
  */
 PDA_API int pda_decode_fused(const pda_plan_t* plan, const void* query, const void* kv_cache,
                              long long num_cache_blocks, const int* block_table, const int* context_lens,
