@@ -47,7 +47,7 @@ L2_FLUSH_BYTES = 512 << 20
 L2_CLEAN_READ_BYTES = 256 << 20
 L2_BYTES = 129e6        # GB300 L2: a step whose KV reads exceed it gets no reuse from one step to the next
 # the files that make up the partition kernel (its ncu counters go stale when one changes)
-PARTITION_KERNEL_SOURCES = ("pda_decode.cuh", "pda_group.cuh", "pda_merge.cuh", "pda_ptx.cuh", "pda_launch.cuh",
+PARTITION_KERNEL_SOURCES = ("pda_decode.cuh", "pda_group.cuh", "pda_rows.cuh", "pda_merge.cuh", "pda_ptx.cuh", "pda_launch.cuh",
                             "pda_internal.h", "pda_decode_bf16.cu", "pda_decode_fp8.cu", "pda_decode_tq4.cu",
                             "pda_api.cu")
 
@@ -64,8 +64,9 @@ def parse():
     ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
-    ap.add_argument("--variant", type=int, default=0, choices=[0, 1, 2],
-                    help="partition-kernel layout for --workload: 0 automatic, 1 head warps, 2 head groups (fp8)")
+    ap.add_argument("--variant", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="partition-kernel layout for --workload: 0 automatic, 1 head warps, 2 head groups (fp8), "
+                         "3 row halves (bf16, QG 16)")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="time only --workload (by default the other configurations are timed too)")
     return ap.parse_args()
@@ -616,7 +617,9 @@ def run_ours(args, rank, world, local_rank):
 
 def kernel_name(pda, p) -> str:
     """The partition kernel pda_decode launches for plan p (its roofline is the line's)."""
-    return "pda_group_kernel" if pda.kernel_variant(p) == pda.VARIANT_HEAD_GROUPS else "pda_partition_kernel"
+    v = pda.kernel_variant(p)
+    return {pda.VARIANT_HEAD_GROUPS: "pda_group_kernel", pda.VARIANT_ROW_HALVES: "pda_rows_kernel"}.get(
+        v, "pda_partition_kernel")
 
 
 def e2e_in_bytes(inp) -> int:

@@ -62,7 +62,7 @@ typedef enum pda_status {
 
 enum { PDA_KV_BF16 = 0, PDA_KV_FP8_E4M3 = 1, PDA_KV_TQ4 = 2 };
 enum { PDA_OUT_BF16 = 0, PDA_OUT_F32 = 1 };
-enum { PDA_VARIANT_AUTO = 0, PDA_VARIANT_HEAD_WARPS = 1, PDA_VARIANT_HEAD_GROUPS = 2 };
+enum { PDA_VARIANT_AUTO = 0, PDA_VARIANT_HEAD_WARPS = 1, PDA_VARIANT_HEAD_GROUPS = 2, PDA_VARIANT_ROW_HALVES = 3 };
 
 /* Bits of the device error word. */
 enum {
@@ -99,13 +99,20 @@ typedef struct pda_plan_t {
     int kernel_variant;            /* how pda_decode lays out the partition pass on the GPU (the
                                       results agree within the parity tolerances; each variant is
                                       deterministic on its own):
-                                        PDA_VARIANT_AUTO (0): chosen at launch from the shape,
+                                        PDA_VARIANT_AUTO (0): chosen at launch from the shape
+                                          (head groups for fp8 and row halves for bf16 with
+                                          query_group_size 16 when the plan has at least two
+                                          units per resident CTA, else head warps),
                                         PDA_VARIANT_HEAD_WARPS (1): one warp per (sequence, KV head,
                                           partition) unit, any format,
                                         PDA_VARIANT_HEAD_GROUPS (2): one CTA per (sequence, group of
-                                          up to 8 KV heads, partition) unit, fp8 e4m3 only.
-                                      pda_decode_fused always uses head warps.  No counterpart on
-                                      the pages.                                                  */
+                                          up to 4 KV heads, partition) unit, fp8 e4m3 only,
+                                        PDA_VARIANT_ROW_HALVES (3): one CTA per (sequence, KV head,
+                                          partition) unit, its 16 query rows split between two
+                                          warps, bf16 with query_group_size 16 only (the
+                                          partials equal head warps' bit for bit).
+                                      pda_decode_fused runs head groups where pda_decode would,
+                                      else head warps.  No counterpart on the pages.              */
     /* ---- outputs of pda_plan ---- */
     int num_partitions;            /* P = ceil(MB*BS / W)                                          */
     int partition_tokens;          /* W = G * 256                                                 */
@@ -272,8 +279,8 @@ PDA_API int pda_decode_step_noalloc(const pda_plan_t* plan, const void* query, c
 
 /*
  * pda_kernel_variant -- host only; launches nothing.  The partition-pass layout pda_decode would
- * launch for this plan on the current device: PDA_VARIANT_HEAD_WARPS or PDA_VARIANT_HEAD_GROUPS
- * (plan->kernel_variant resolved, PDA_VARIANT_AUTO included).  Returns PDA_ERR_INVALID_ARG for
+ * launch for this plan on the current device: PDA_VARIANT_HEAD_WARPS, PDA_VARIANT_HEAD_GROUPS or
+ * PDA_VARIANT_ROW_HALVES (plan->kernel_variant resolved, PDA_VARIANT_AUTO included).  Returns PDA_ERR_INVALID_ARG for
  * a NULL or edited plan, PDA_ERR_CUDA when the device cannot be queried.  No counterpart on the
  * pages.
  */

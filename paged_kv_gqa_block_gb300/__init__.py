@@ -35,6 +35,7 @@ HEAD_DIM = 128
 VARIANT_AUTO = 0
 VARIANT_HEAD_WARPS = 1
 VARIANT_HEAD_GROUPS = 2
+VARIANT_ROW_HALVES = 3
 
 STATUS = {0: "PDA_OK", -1: "PDA_ERR_INVALID_ARG", -2: "PDA_ERR_UNSUPPORTED", -3: "PDA_ERR_WORKSPACE_TOO_SMALL",
           -4: "PDA_ERR_LAUNCH", -5: "PDA_ERR_NOT_IMPLEMENTED", -6: "PDA_ERR_CUDA"}
@@ -125,7 +126,7 @@ def plan(num_seqs: int, num_kv_heads: int, query_group_size: int, kv_block_size:
 
 def kernel_variant(p: Plan) -> int:
     """pda_kernel_variant: the partition-pass layout pda_decode launches for this plan on the
-    current device (VARIANT_HEAD_WARPS or VARIANT_HEAD_GROUPS)."""
+    current device (VARIANT_HEAD_WARPS, VARIANT_HEAD_GROUPS or VARIANT_ROW_HALVES)."""
     rc = lib().pda_kernel_variant(ctypes.byref(p))
     if rc < 0:
         raise PdaError(rc, "pda_kernel_variant")

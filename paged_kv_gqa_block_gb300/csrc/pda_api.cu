@@ -165,7 +165,7 @@ static int compute_plan(const pda_plan_t* in, pda_plan_t* out) {
     *out = *in;
     if (in->num_seqs < 0 || in->num_kv_heads < 1 || in->max_blocks_per_seq < 1 || in->tile_groups_per_partition < 0 ||
         in->max_partitions < 0 || in->wait_timeout_ns < 0 || in->kernel_variant < PDA_VARIANT_AUTO ||
-        in->kernel_variant > PDA_VARIANT_HEAD_GROUPS)
+        in->kernel_variant > PDA_VARIANT_ROW_HALVES)
         return PDA_ERR_INVALID_ARG;
     if (in->query_group_size != 6 && in->query_group_size != 8 && in->query_group_size != 16)
         return PDA_ERR_UNSUPPORTED;
@@ -174,6 +174,8 @@ static int compute_plan(const pda_plan_t* in, pda_plan_t* out) {
     if (in->kv_dtype != PDA_KV_BF16 && in->kv_dtype != PDA_KV_FP8_E4M3 && in->kv_dtype != PDA_KV_TQ4)
         return PDA_ERR_UNSUPPORTED;
     if (in->kernel_variant == PDA_VARIANT_HEAD_GROUPS && in->kv_dtype != PDA_KV_FP8_E4M3) return PDA_ERR_UNSUPPORTED;
+    if (in->kernel_variant == PDA_VARIANT_ROW_HALVES && (in->kv_dtype != PDA_KV_BF16 || in->query_group_size != 16))
+        return PDA_ERR_UNSUPPORTED;
     if (!std::isfinite(in->softmax_scale)) return PDA_ERR_INVALID_ARG;
     const long long max_ctx = (long long)in->max_blocks_per_seq * in->kv_block_size;
     if (max_ctx > (1ll << 30)) return PDA_ERR_INVALID_ARG;   // context lengths are int32
@@ -243,6 +245,15 @@ static bool use_head_groups(const pda_plan_t* plan) {
     return units >= 2ll * 2 * device_sm_count();
 }
 
+// Row halves (bf16, QG 16) when asked for, or, with PDA_VARIANT_AUTO, when the plan has room for
+// at least two (sequence, KV head, partition) units per resident row-half CTA (four per SM).
+static bool use_row_halves(const pda_plan_t* plan) {
+    if (plan->kernel_variant != PDA_VARIANT_AUTO) return plan->kernel_variant == PDA_VARIANT_ROW_HALVES;
+    if (plan->kv_dtype != PDA_KV_BF16 || plan->query_group_size != 16) return false;
+    const long long units = (long long)plan->num_seqs * plan->num_kv_heads * plan->num_partitions;
+    return units >= 2ll * 4 * device_sm_count();
+}
+
 // The partition pass; with `fused`, the same (cooperative) launch also combines the partials
 // into `out` after a grid barrier (`counters` is reserved and left untouched).
 static int decode_launch(const pda_plan_t* plan, const void* query, const void* kv_cache, long long num_cache_blocks,
@@ -302,6 +313,7 @@ static int decode_launch(const pda_plan_t* plan, const void* query, const void* 
         return launch_decode_fp8_groups(a, kv_map, sc_map, fused, s);
     }
     if (!encode_kv_map(&kv_map, kv_cache, plan, num_cache_blocks)) return PDA_ERR_LAUNCH;
+    if (plan->kv_dtype == PDA_KV_BF16 && !fused && use_row_halves(plan)) return launch_decode_bf16_rows(a, kv_map, s);
     if (plan->kv_dtype == PDA_KV_BF16) return launch_decode_bf16(a, kv_map, fused, s);
     if (!encode_scale_map(&sc_map, kv_cache, plan, num_cache_blocks)) return PDA_ERR_LAUNCH;
     if (tq) return launch_decode_tq4(a, kv_map, sc_map, s);
@@ -383,8 +395,10 @@ int pda_plan_struct_size(void) { return (int)sizeof(pda_plan_t); }
 
 int pda_kernel_variant(const pda_plan_t* plan) {
     if (!plan || !plan_matches(plan)) return PDA_ERR_INVALID_ARG;
-    if (plan->kv_dtype != PDA_KV_FP8_E4M3) return PDA_VARIANT_HEAD_WARPS;
+    const bool rows_possible = plan->kv_dtype == PDA_KV_BF16 && plan->query_group_size == 16;
+    if (plan->kv_dtype != PDA_KV_FP8_E4M3 && !rows_possible) return PDA_VARIANT_HEAD_WARPS;
     if (plan->kernel_variant == PDA_VARIANT_AUTO && device_sm_count() <= 0) return PDA_ERR_CUDA;
+    if (rows_possible) return use_row_halves(plan) ? PDA_VARIANT_ROW_HALVES : PDA_VARIANT_HEAD_WARPS;
     return use_head_groups(plan) ? PDA_VARIANT_HEAD_GROUPS : PDA_VARIANT_HEAD_WARPS;
 }
 

@@ -226,7 +226,9 @@ __device__ inline void find_range(const DecodeArgs& a, UnitIt& u, long long& hi)
 }
 
 // ---------------------------------------------------------------------------------------------
-template <int KV, int NT, int S, bool FUSED>
+// EAGER: the eager softmax update even where kLazy would apply (the QG = 16 row-half kernel,
+// whose 8-row blocks must give the bits of this kernel's two n-tiles).
+template <int KV, int NT, int S, bool FUSED, bool EAGER = false>
 struct Decode {
     using Cfg = DecodeCfg<KV, S>;
     static constexpr bool FP8 = KV == PDA_KV_FP8_E4M3;
@@ -433,7 +435,7 @@ struct Decode {
     // step's largest V weight).  That order is kept where the lazy form measured slower: the fp8
     // kernel, whose 168-register budget (12 CTAs per SM) it strains, and QG = 16 (two n-tiles).
     static constexpr float kLazyLog2 = 8.f;
-    static constexpr bool kLazy = NT == 1 && !FP8;
+    static constexpr bool kLazy = NT == 1 && !FP8 && !EAGER;
     template <int NTL, bool VS, bool ZS>
     static __device__ __forceinline__ void softmax_step(float (&s)[NTL][NT][4], float (&w0)[NTL], float (&w1)[NTL],
                                                         const float (&z0)[NTL], const float (&z1)[NTL],

@@ -51,6 +51,8 @@ struct ReduceArgs {
 int launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& kv_map, bool fused, cudaStream_t stream);
 int launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kv_map, const CUtensorMap& sc_map, bool fused,
                       cudaStream_t stream);
+// The row-half kernel (bf16, QG 16): two consumer warps of 8 query rows per CTA.
+int launch_decode_bf16_rows(const DecodeArgs& a, const CUtensorMap& kv_map, cudaStream_t stream);
 // The head-group kernel (fp8): a.HG heads per CTA; the maps' boxes span a.HG heads.
 // With `fused`, the same (cooperative) launch also combines the partials into `out` after a
 // grid barrier.

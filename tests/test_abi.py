@@ -73,8 +73,10 @@ def test_plan_worked_example(pda):
     (dict(kv_block_size=64), -2), (dict(head_dim=64), -2), (dict(kv_dtype=3), -2), (dict(kv_dtype=-1), -2),
     (dict(num_kv_heads=0), -1), (dict(max_blocks_per_seq=0), -1), (dict(tile_groups_per_partition=-1), -1),
     (dict(num_seqs=-1), -1), (dict(max_partitions=-2), -1), (dict(softmax_scale=float("nan")), -1),
-    (dict(wait_timeout_ns=-1), -1), (dict(kernel_variant=-1), -1), (dict(kernel_variant=3), -1),
+    (dict(wait_timeout_ns=-1), -1), (dict(kernel_variant=-1), -1), (dict(kernel_variant=4), -1),
     (dict(kernel_variant=2), -2), (dict(kernel_variant=2, kv_dtype=2), -2),
+    (dict(kernel_variant=3), -2), (dict(kernel_variant=3, query_group_size=16, kv_dtype=1), -2),
+    (dict(kernel_variant=3, query_group_size=16, kv_dtype=2), -2),
 ])
 def test_plan_rejects(pda, kw, code):
     args = dict(num_seqs=2, num_kv_heads=2, query_group_size=8, kv_block_size=16, max_blocks_per_seq=4)
@@ -141,6 +143,13 @@ def test_head_group_variant_is_accepted_for_fp8(pda):
     for v in (0, 1, 2):
         p = pda.plan(2, 8, 6, 16, 4, kv_dtype=pda.KV_FP8_E4M3, kernel_variant=v)
         assert p.kernel_variant == v
+
+
+def test_row_half_variant_is_accepted_for_bf16_with_sixteen_rows(pda):
+    for v, want in ((1, pda.VARIANT_HEAD_WARPS), (3, pda.VARIANT_ROW_HALVES)):
+        p = pda.plan(2, 4, 16, 32, 4, kv_dtype=pda.KV_BF16, kernel_variant=v)
+        assert p.kernel_variant == v
+        assert pda.kernel_variant(p) == want
 
 
 def test_kernel_variant_of_a_plan(pda):

@@ -107,7 +107,14 @@ SWEEP += [
     (wl.KV_FP8_E4M3, 8, 32, 1, 12, (300, 901)),
     (wl.KV_FP8_E4M3, 6, 16, 1, 5, (64, 777)),
 ]
-SWEEP_CASES = [(*c, v) for c in SWEEP for v in ((1, 2) if c[0] == wl.KV_FP8_E4M3 else (0,))]
+def _variants(kv, QG):
+    # fp8 on both of its kernels; bf16 with sixteen rows on head warps (automatic) and row halves
+    if kv == wl.KV_FP8_E4M3:
+        return (1, 2)
+    return (0, 3) if kv == wl.KV_BF16 and QG == 16 else (0,)
+
+
+SWEEP_CASES = [(*c, v) for c in SWEEP for v in _variants(c[0], c[1])]
 
 
 @pytest.mark.parametrize("kv,QG,BS,G,Hk,ctx,variant", SWEEP_CASES)
@@ -361,7 +368,8 @@ def test_bad_block_id_sets_error_bit_without_faulting():
 
 # ---------------------------------------------------------------- full-size workloads
 FULL_CASES = [(n, 0) for n in wl.WORKLOAD_ORDER] + [
-    (n, v) for n in wl.WORKLOAD_ORDER if wl.WORKLOADS[n].kv_dtype == wl.KV_FP8_E4M3 for v in (1, 2)]
+    (n, v) for n in wl.WORKLOAD_ORDER for v in _variants(wl.WORKLOADS[n].kv_dtype, wl.WORKLOADS[n].query_group_size)
+    if v != 0]
 
 
 @pytest.mark.parametrize("name,variant", FULL_CASES)
@@ -374,6 +382,57 @@ def test_full_size_workload_every_unit(oracle_mod, name, variant):
     assert res["err"] == 0
     assert np.isfinite(res["out"]).all()
     check_against_oracle(inp, res, oh.run_oracle(inp, partials=True))
+
+
+ROW_HALF_CASES = [
+    ("b32_hk4_qg16_bs32_ctx2048-8192_kbias", None),
+    # long and short sequences, an empty one, one of a single partial tile, BS 16 and 32, G 1 and 2
+    (None, dict(num_seqs=6, num_kv_heads=2, query_group_size=16, kv_block_size=16, ctx=(5000, 1, 0, 700, 257, 4097),
+                seed=131)),
+    (None, dict(num_seqs=3, num_kv_heads=3, query_group_size=16, kv_block_size=32, ctx=(2049, 64, 9000),
+                tile_groups_per_partition=2, seed=132)),
+]
+
+
+@pytest.mark.parametrize("name,kw", ROW_HALF_CASES)
+def test_row_halves_equal_head_warps_bit_for_bit(oracle_mod, name, kw):
+    # The row-half kernel runs each 8-row block with the head-warp kernel's arithmetic: the same
+    # partials (and so the same outputs), bit for bit, written to the same partitions.
+    w = wl.WORKLOADS[name] if name else wl.small(kv_dtype=wl.KV_BF16, extra_blocks=3, **kw)
+    inp = wl.generate(w)
+    d = to_device(inp)
+    head, rows = run_gpu(inp, d=d, variant=1), run_gpu(inp, d=d, variant=3)
+    assert head["err"] == 0 and rows["err"] == 0
+    for k in ("part_o", "part_m", "part_l"):
+        assert np.array_equal(head[k].view(np.int32), rows[k].view(np.int32)), k
+    assert np.array_equal(head["out"], rows["out"])
+    check_against_oracle(inp, rows, oh.run_oracle(inp, partials=True))
+
+
+def test_row_half_counters_return_to_zero_across_many_launches(oracle_mod):
+    # the row-half kernel takes units from the library's counter slots too: 300 launches in a row
+    # (every slot reused) give the first launch's bits
+    import paged_kv_gqa_block_gb300 as pda
+    from tests.gpu_helpers import plan_for, sentinel_ws
+    w = wl.small(num_seqs=4, num_kv_heads=4, query_group_size=16, kv_block_size=16, ctx=(3000, 17, 600, 2048),
+                 kv_dtype=wl.KV_BF16, seed=133)
+    inp = wl.generate(w)
+    d = to_device(inp)
+    p = plan_for(w, variant=3)
+    ws = sentinel_ws(p)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for i in range(300):
+        pda.decode(p, d["query"], d["cache"], w.num_cache_blocks, d["block_table"], d["context_lens"],
+                   ws["partial_out"], ws["exp_sums"], ws["max_logits"], err_word=err)
+        if i in (0, 299):
+            o = torch.empty((w.num_seqs, w.num_q_heads, 128), dtype=torch.float32, device="cuda")
+            pda.reduce(p, d["context_lens"], ws["partial_out"], ws["exp_sums"], ws["max_logits"], o, err_word=err)
+            outs.append(o.cpu().numpy())
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(outs[0].view(np.int32), outs[1].view(np.int32))
+    assert np.abs(outs[0] - oh.run_oracle(inp)["out"]).max() <= TOL[wl.KV_BF16]
 
 
 def test_head_group_counters_return_to_zero_across_many_launches(oracle_mod):
@@ -405,10 +464,13 @@ def test_head_group_counters_return_to_zero_across_many_launches(oracle_mod):
 
 def test_automatic_variant_on_the_full_size_workloads():
     # the fp8 configuration (64 sequences, 8 heads: head groups of 4, 256 units of room per group)
-    # runs on head groups; every other format runs on head warps
+    # runs on head groups, the bf16 QG 16 configuration (4 096 units) on row halves; the others
+    # run on head warps
     import paged_kv_gqa_block_gb300 as pda
     from tests.gpu_helpers import plan_for
     for name in wl.WORKLOAD_ORDER:
         w = wl.WORKLOADS[name]
-        want = pda.VARIANT_HEAD_GROUPS if w.kv_dtype == wl.KV_FP8_E4M3 else pda.VARIANT_HEAD_WARPS
+        want = (pda.VARIANT_HEAD_GROUPS if w.kv_dtype == wl.KV_FP8_E4M3 else
+                pda.VARIANT_ROW_HALVES if w.kv_dtype == wl.KV_BF16 and w.query_group_size == 16 else
+                pda.VARIANT_HEAD_WARPS)
         assert pda.kernel_variant(plan_for(w)) == want, name
