@@ -48,3 +48,25 @@ def test_timing_mode_follows_the_kv_bytes_against_l2():
         note = bench.l2_note(mode, w, inp, W)
         assert ("back to back" in note) == (mode == "back_to_back")
         assert note.startswith("flushed") == (mode == "flushed")
+
+
+def test_roofline_kernel_name_follows_the_variant():
+    # the line's roofline names the kernel pda_decode launches for the plan (its ncu traffic entry
+    # is looked up under that workload)
+    import bench
+    pda = types.SimpleNamespace(VARIANT_HEAD_WARPS=1, VARIANT_HEAD_GROUPS=2, VARIANT_ROW_HALVES=3)
+    for v, want in ((1, "pda_partition_kernel"), (2, "pda_group_kernel"), (3, "pda_rows_kernel")):
+        pda.kernel_variant = lambda p, v=v: v
+        assert bench.kernel_name(pda, None) == want
+
+
+def test_kernel_source_hash_covers_every_partition_kernel_source():
+    # a change to any translation unit or header of the partition kernels must change the hash that
+    # gates the committed DRAM traffic figures
+    import glob
+    import os
+    import bench
+    csrc = os.path.join(os.path.dirname(bench.__file__), "paged_kv_gqa_block_gb300", "csrc")
+    kernel_files = {os.path.basename(f) for f in glob.glob(os.path.join(csrc, "*.cu*")) + glob.glob(os.path.join(csrc, "*.h"))}
+    # the write side and the no-allocation wrapper launch no partition kernel of their own
+    assert kernel_files - set(bench.PARTITION_KERNEL_SOURCES) <= {"pda_append.cu", "pda_noalloc.cu"}
